@@ -1,0 +1,333 @@
+// C ABI of the DSA decode path (declared in include/dsa.h): host-side argument
+// validation, per-device state (SM count, device error word) and dispatch to
+// the kernel launchers.  Every check runs before anything is enqueued; there is
+// no fallback path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "dsa.h"
+#include "internal.h"
+
+namespace dsa {
+namespace {
+
+thread_local char g_msg[512] = "";
+
+dsa_status fail(dsa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+dsa_status ok() {
+  g_msg[0] = '\0';
+  return DSA_OK;
+}
+
+// One error word per device: the library's only device-resident state.
+__device__ uint32_t g_err_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* info) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.device != dev) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return e;
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_err_word);
+    if (e != cudaSuccess) return e;
+    d.sm_count = prop.multiProcessorCount;
+    d.cc_major = prop.major;
+    d.cc_minor = prop.minor;
+    d.smem_optin = prop.sharedMemPerBlockOptin;
+    d.err_word = static_cast<uint32_t*>(addr);
+    d.device = dev;
+  }
+  *info = d;
+  return cudaSuccess;
+}
+
+bool encode_tensor_map(void* map_out, int dtype, int rank, void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128,
+                       char* msg, size_t msg_len) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) {
+    snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
+    return false;
+  }
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
+  const CUtensorMapDataType dt =
+      dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), dt, static_cast<cuuint32_t>(rank),
+                        base, d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+namespace {
+
+// Device checks shared by every entry point.
+dsa_status device_ready(DeviceInfo* dev) {
+  cudaError_t e = current_device_info(dev);
+  if (e != cudaSuccess)
+    return fail(DSA_ERR_CUDA, "no usable CUDA device: %s", cudaGetErrorString(e));
+  if (!(dev->cc_major == 10 && dev->cc_minor == 3))
+    return fail(DSA_ERR_UNSUPPORTED,
+                "this library is built for sm_103a (GB300); the current device is sm_%d%d",
+                dev->cc_major, dev->cc_minor);
+  return DSA_OK;
+}
+
+dsa_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_version(void) { return 100; }
+
+const char* dsa_last_error(void) { return g_msg; }
+
+dsa_status dsa_get_device_error(void* stream, uint32_t* bits, int clear) {
+  if (!bits) return fail(DSA_ERR_INVALID_ARG, "dsa_get_device_error: bits is NULL");
+  DeviceInfo dev;
+  cudaError_t e = current_device_info(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "dsa_get_device_error");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  e = cudaMemcpyAsync(&host, dev.err_word, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) {
+    e = cudaMemsetAsync(dev.err_word, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return cuda_status(e, "dsa_get_device_error");
+  *bits = host;
+  return ok();
+}
+
+dsa_status dsa_indexer_logits(const uint8_t* q_fp8, const float* q_scale, const float* weights,
+                              const uint8_t* k_cache, int64_t k_page_stride,
+                              const uint8_t* k_scale, int64_t s_page_stride, int num_pages,
+                              const int32_t* block_table, int64_t bt_stride,
+                              const int32_t* ctx_len, int num_req, int next_n, float* logits,
+                              int64_t ld, void* stream) {
+  const char* fn = "dsa_indexer_logits";
+  if (!q_fp8 || !q_scale || !weights || !k_cache || !k_scale || !block_table || !ctx_len ||
+      !logits)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (num_req < 0 || next_n < 1 || next_n > 65536 || num_pages < 1 || bt_stride < 1 || ld < 4)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: bad sizes (num_req=%d next_n=%d num_pages=%d bt_stride=%lld ld=%lld)", fn,
+                num_req, next_n, num_pages, (long long)bt_stride, (long long)ld);
+  if (static_cast<int64_t>(num_req) * next_n * 64 > (1ll << 31) - 1)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: too many query rows", fn);
+  if (num_req > 4096) return fail(DSA_ERR_UNSUPPORTED, "%s: num_req > 4096", fn);
+  if (k_page_stride < 64 * 128 || k_page_stride % 16 || s_page_stride < 256 ||
+      s_page_stride % 16)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: page strides must cover the page payload and be multiples of 16 bytes", fn);
+  if (!aligned16(k_cache) || !aligned16(k_scale) || !aligned16(q_fp8) || !aligned16(logits) ||
+      ld % 4)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: k_cache, k_scale, q_fp8 and logits must be 16-byte aligned, ld %% 4 == 0", fn);
+  if (num_req == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  IndexerArgs a{q_fp8,     q_scale,     weights,   k_cache, k_page_stride, k_scale, s_page_stride,
+                num_pages, block_table, bt_stride, ctx_len, num_req,       next_n,  logits,
+                ld};
+  char msg[256] = "";
+  cudaError_t e = launch_indexer(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
+  if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
+  return cuda_status(e, fn);
+}
+
+dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
+                    const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
+                    int force_path, void* stream) {
+  const char* fn = "dsa_topk";
+  if (!logits || !row_len || !out_idx)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (R < 0 || k < 1 || k > DSA_MAX_TOPK || ld < 4 || ld % 4 || !aligned16(logits))
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: need R >= 0, 1 <= k <= %d, ld %% 4 == 0, 16-byte aligned logits", fn,
+                DSA_MAX_TOPK);
+  if (ld > (1ll << 31) - 1) return fail(DSA_ERR_UNSUPPORTED, "%s: rows longer than 2^31", fn);
+  if (col_blocks && (nb < 1 || block_size < 1))
+    return fail(DSA_ERR_INVALID_ARG, "%s: col_blocks needs nb >= 1 and block_size >= 1", fn);
+  if (force_path < 0 || force_path > 2)
+    return fail(DSA_ERR_INVALID_ARG, "%s: force_path must be 0, 1 or 2", fn);
+  if (R == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  TopkArgs a{logits, ld, row_len, R, k, col_blocks, nb, block_size, out_idx, force_path};
+  return cuda_status(launch_topk(a, dev, static_cast<cudaStream_t>(stream)), fn);
+}
+
+size_t dsa_sparse_mla_workspace_size(int R, int k) {
+  if (R <= 0 || k <= 0) return 0;
+  return mla_workspace_size(R, k);
+}
+
+dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache,
+                                 int64_t kv_page_stride, int num_pages,
+                                 const int32_t* block_table, int64_t bt_stride, int num_req,
+                                 int next_n, const int32_t* idx, int k, float sm_scale,
+                                 uint16_t* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  const char* fn = "dsa_sparse_mla_decode";
+  if (!q || !kv_cache || !block_table || !idx || !out)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (num_req < 0 || next_n < 1 || num_pages < 1 || bt_stride < 1 || k < 1 ||
+      k > DSA_MAX_TOPK || !(sm_scale > 0.f))
+    return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes or scale", fn);
+  if (kv_page_stride < 64 * 576 * 2 || kv_page_stride % 16 || !aligned16(kv_cache) ||
+      !aligned16(q) || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: kv page stride must be >= 73728 and a multiple of 16; q, kv and out "
+                "16-byte aligned",
+                fn);
+  const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
+  if (R64 > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
+  const int R = static_cast<int>(R64);
+  if (R == 0) return ok();
+  const size_t need = mla_workspace_size(R, k);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace_bytes);
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  MlaArgs a{q,   kv_cache, kv_page_stride, num_pages, block_table, bt_stride, num_req, next_n,
+            idx, k,        sm_scale,       out,       lse,         workspace, workspace_bytes};
+  return cuda_status(launch_sparse_mla(a, dev, static_cast<cudaStream_t>(stream)), fn);
+}
+
+size_t dsa_candidate_schedule_size(int R) {
+  if (R <= 0) return 0;
+  return candidate_schedule_size(R);
+}
+
+dsa_status dsa_candidate_expand(const int32_t* cand, int R, int nb, int block_size,
+                                const int32_t* ctx_len, int next_n, int32_t* sparse_indices,
+                                int32_t* end, void* schedule, size_t schedule_bytes,
+                                void* stream) {
+  const char* fn = "dsa_candidate_expand";
+  if (!cand || !ctx_len || !sparse_indices || !end || !schedule)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (R < 0 || nb < 1 || next_n < 1 || (R % next_n) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "%s: need nb >= 1, next_n >= 1, R %% next_n == 0", fn);
+  if (block_size != DSA_PAGE_TOKENS)
+    return fail(DSA_ERR_UNSUPPORTED,
+                "%s: candidate_block_size must equal the %d-token page (got %d)", fn,
+                DSA_PAGE_TOKENS, block_size);
+  if (nb > 4096) return fail(DSA_ERR_UNSUPPORTED, "%s: nb > 4096 candidate blocks", fn);
+  if (schedule_bytes < candidate_schedule_size(R))
+    return fail(DSA_ERR_WORKSPACE, "%s: schedule needs %zu bytes", fn,
+                candidate_schedule_size(R));
+  if (R == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  CandExpandArgs a{cand, R, nb, block_size, ctx_len, next_n, sparse_indices, end, schedule};
+  return cuda_status(launch_candidate_expand(a, dev, static_cast<cudaStream_t>(stream)), fn);
+}
+
+dsa_status dsa_candidate_logits(const uint8_t* q_fp8, const float* q_scale, const float* weights,
+                                const uint8_t* k_fp4, int64_t k_page_stride, const uint8_t* k_sf,
+                                int64_t sf_page_stride, int num_pages,
+                                const int32_t* block_table, int64_t bt_stride, int num_req,
+                                int next_n, const int32_t* sparse_indices, int nb,
+                                int block_size, const int32_t* end, const void* schedule,
+                                size_t schedule_bytes, float* logits, int64_t ld, void* stream) {
+  const char* fn = "dsa_candidate_logits";
+  if (!q_fp8 || !q_scale || !weights || !k_fp4 || !k_sf || !block_table || !sparse_indices ||
+      !end || !schedule || !logits)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (num_req < 0 || next_n < 1 || num_pages < 1 || bt_stride < 1 || nb < 1)
+    return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes", fn);
+  if (block_size != DSA_PAGE_TOKENS)
+    return fail(DSA_ERR_UNSUPPORTED,
+                "%s: candidate_block_size must equal the %d-token page (got %d)", fn,
+                DSA_PAGE_TOKENS, block_size);
+  if (k_page_stride < 64 * 64 || k_page_stride % 16 || sf_page_stride < 256 ||
+      sf_page_stride % 16 || !aligned16(k_fp4) || !aligned16(k_sf) || !aligned16(q_fp8) ||
+      !aligned16(logits) || ld % 4 || ld < static_cast<int64_t>(nb) * block_size)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: strides must be multiples of 16, buffers 16-byte aligned, ld >= nb*bs and "
+                "ld %% 4 == 0",
+                fn);
+  const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
+  if (R64 > (1 << 20)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
+  const int R = static_cast<int>(R64);
+  if (schedule_bytes < candidate_schedule_size(R))
+    return fail(DSA_ERR_WORKSPACE, "%s: schedule needs %zu bytes", fn,
+                candidate_schedule_size(R));
+  if (R == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  CandLogitsArgs a{q_fp8,          q_scale,   weights,     k_fp4,     k_page_stride, k_sf,
+                   sf_page_stride, num_pages, block_table, bt_stride, num_req,       next_n,
+                   sparse_indices, nb,        block_size,  end,       schedule,      logits,
+                   ld};
+  char msg[256] = "";
+  cudaError_t e =
+      launch_candidate_logits(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
+  if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
+  return cuda_status(e, fn);
+}
+
+}  // extern "C"

@@ -1,0 +1,472 @@
+// Lightning-indexer logits over a paged FP8 key cache, Eq. (1) of "DeepSeek
+// V3.2-Exp support" (llama.cpp issue 16331, section "1. Architecture"):
+//
+//   logits[r, t] = s_t * sum_h (w[r,h] * sq[r,h]) * ReLU(q'[r,h] . k'_t)
+//
+// One persistent CTA per SM walks a contiguous range of work chunks
+// (a chunk = up to kChunkTiles tiles of 128 tokens of one row group; a row
+// group = up to 4 query rows of one request, which read the same keys).
+//
+//   warp 0      TMA producer: two 64-token key pages per tile
+//               (cp.async.bulk.tensor, 128-byte swizzle) + their 2 x 256 B
+//               of per-token scales (cp.async.bulk); the group's q (one 2-D
+//               TMA box of N = 64*rows rows) and w*sq into a Q slot.
+//   warp 1      tcgen05 issuer: D[128 tokens, N] = K[128, 128] * Q[N, 128]^T,
+//               four kind::f8f6f4 MMAs (K = 32 each) into one of two TMEM
+//               accumulators.
+//   warps 2-9   two epilogue warpgroups, one per TMEM accumulator: each
+//               thread owns one token (one TMEM lane) and reduces
+//               sum_h w'_h * max(d_h, 0) per row, times s_t, and stores the
+//               row's logit (consecutive threads -> consecutive tokens).
+//
+// Decode (1-2 rows per group) is bound by the HBM read of the key cache
+// (132 B per token); a prefill chunk (4 rows per group, N = 256) is bound by
+// the tensor pipe and the epilogue ALU.
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kStages = 8;
+constexpr int kTileTokens = 128;
+constexpr uint32_t kPageKeyBytes = 64 * 128;  // 8192
+constexpr uint32_t kStageBytes = 2 * kPageKeyBytes;
+constexpr int kChunkTiles = 4;
+constexpr int kMaxReq = 4096;
+
+struct KParams {
+  const float* q_scale;
+  const float* w;
+  const uint8_t* k_scale;
+  int64_t s_page_stride;
+  int num_pages;
+  const int32_t* bt;
+  int64_t bt_stride;
+  const int32_t* ctx_len;
+  int num_req;
+  int next_n;
+  float* logits;
+  int64_t ld;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int group_tiles(int ctx, int next_n, int G, int gsub) {
+  const int jlast = min(gsub * G + G, next_n) - 1;
+  const int L = ctx - (next_n - 1 - jlast);
+  return L <= 0 ? 0 : div_up(L, kTileTokens);
+}
+
+// Walks the chunks [c, c_end) of this CTA in order.  Every role runs an
+// identical cursor, so they agree on the sequence of (group, tile range)
+// without talking to each other.
+struct Cursor {
+  const int* prefix;  // smem [num_req + 1] exclusive chunk prefix per request
+  const int32_t* ctx_len;
+  int num_req, next_n, G, ngroups;
+  int c, c_end;
+  int req, gsub, ctx, tiles, gchunk, nchunk;
+  int gcount;  // groups entered so far (the current group's Q slot is gcount & 1)
+
+  __device__ void enter_group() {
+    tiles = group_tiles(ctx, next_n, G, gsub);
+    nchunk = div_up(tiles, kChunkTiles);
+  }
+  // Moves to the first group with chunks at or after (req, gsub).
+  __device__ void settle() {
+    for (;;) {
+      if (req >= num_req) return;
+      if (gsub >= ngroups || prefix[req + 1] == prefix[req]) {
+        ++req;
+        gsub = 0;
+        if (req < num_req) ctx = ctx_len[req];
+        continue;
+      }
+      enter_group();
+      if (nchunk > 0) return;
+      ++gsub;
+    }
+  }
+  __device__ void init(const int* pre, const int32_t* ctxs, int nreq, int nn, int g, int c0,
+                       int c1) {
+    prefix = pre;
+    ctx_len = ctxs;
+    num_req = nreq;
+    next_n = nn;
+    G = g;
+    ngroups = div_up(nn, g);
+    c = c0;
+    c_end = c1;
+    gcount = 0;
+    if (c >= c_end) return;
+    int lo = 0, hi = num_req;  // largest req with prefix[req] <= c
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= c) lo = mid; else hi = mid;
+    }
+    req = lo;
+    ctx = ctx_len[req];
+    int rem = c - prefix[req];
+    gsub = 0;
+    for (;;) {
+      enter_group();
+      if (rem < nchunk) break;
+      rem -= nchunk;
+      ++gsub;
+    }
+    gchunk = rem;
+  }
+  __device__ bool valid() const { return c < c_end; }
+  __device__ int tile_begin() const { return gchunk * kChunkTiles; }
+  __device__ int tile_end() const { return min(tiles, gchunk * kChunkTiles + kChunkTiles); }
+  __device__ int row0() const { return req * next_n + gsub * G; }
+  __device__ int nrows() const { return min(G, next_n - gsub * G); }
+  // Advances to the next chunk; returns true if it leaves the current group.
+  __device__ bool next() {
+    ++c;
+    if (c >= c_end) return true;
+    if (++gchunk < nchunk) return false;
+    gchunk = 0;
+    ++gsub;
+    settle();
+    ++gcount;
+    return true;
+  }
+  // Row length of row j of the current group.
+  __device__ int row_len(int j) const {
+    const int jj = gsub * G + j;
+    return max(0, ctx - (next_n - 1 - jj));
+  }
+};
+
+template <int G>
+struct Smem {
+  static constexpr int N = 64 * G;
+  static constexpr uint32_t kQBytes = N * 128;
+  uint8_t keys[kStages][kStageBytes];  // 1024-aligned stage tiles
+  uint8_t q[2][kQBytes];
+  float scales[kStages][kTileTokens];
+  float wq[2][N];
+  int prefix[kMaxReq + 1];
+  uint64_t full[kStages], empty[kStages];
+  uint64_t qfull[2], qempty[2];
+  uint64_t tfull[2], tempty[2];
+  uint32_t tmem_base;
+  int abort;
+  int scan_tmp[kThreads];
+};
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                   const KParams p) {
+  constexpr int N = 64 * G;
+  constexpr uint32_t kTmemCols = (2 * N <= 128) ? 128 : (2 * N <= 256 ? 256 : 512);
+  constexpr uint32_t kIdesc = make_idesc(0, 0, 128, N, false, false);
+  using S = Smem<G>;
+  extern __shared__ uint8_t smem_raw[];
+  S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- per-request chunk counts and their exclusive prefix (all threads) ----
+  const int ngroups = div_up(p.next_n, G);
+  for (int i = tid; i < p.num_req; i += kThreads) {
+    const int ctx = p.ctx_len[i];
+    int n = 0;
+    for (int g = 0; g < ngroups; ++g) n += div_up(group_tiles(ctx, p.next_n, G, g), kChunkTiles);
+    s.prefix[i + 1] = n;
+  }
+  if (tid == 0) {
+    s.prefix[0] = 0;
+    s.abort = 0;
+  }
+  __syncthreads();
+  {
+    // Each thread sums a contiguous segment; one warp scans the partials.
+    const int n = p.num_req;
+    const int seg = div_up(n, kThreads);
+    const int a = min(n, tid * seg), b = min(n, a + seg);
+    int sum = 0;
+    for (int i = a; i < b; ++i) sum += s.prefix[i + 1];
+    s.scan_tmp[tid] = sum;
+    __syncthreads();
+    if (warp == 0) {
+      constexpr int per = kThreads / 32;
+      int loc[per];
+      int tot = 0;
+#pragma unroll
+      for (int i = 0; i < per; ++i) {
+        loc[i] = s.scan_tmp[lane * per + i];
+        tot += loc[i];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - tot;
+#pragma unroll
+      for (int i = 0; i < per; ++i) {
+        s.scan_tmp[lane * per + i] = run;
+        run += loc[i];
+      }
+    }
+    __syncthreads();
+    int run = s.scan_tmp[tid];
+    for (int i = a; i < b; ++i) {
+      run += s.prefix[i + 1];
+      s.prefix[i + 1] = run;
+    }
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1 + 4);  // MMA commit + the 4 epilogue warps that read the scales
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.qfull[i], 32);     // the 32 producer lanes (w*sq) + TMA bytes
+      mbar_init(&s.qempty[i], 1 + 8); // MMA commit + 8 epilogue warps
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int total = s.prefix[p.num_req];
+  const int c0 = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
+  const int c1 = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
+  volatile int* abort = &s.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    Cursor cur;
+    cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_q);
+    }
+    int lt = 0;  // local tile counter
+    bool new_group = true;
+    while (cur.valid() && !*abort) {
+      const int r0 = cur.row0();
+      const int nr = cur.nrows();
+      if (new_group) {
+        const int slot = cur.gcount & 1;
+        const int use = cur.gcount >> 1;
+        if (use > 0 && !mbar_wait(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
+        for (int i = lane; i < N; i += 32) {
+          const int j = i >> 6, h = i & 63;
+          float v = 0.f;
+          if (j < nr) v = p.w[(r0 + j) * 64 + h] * p.q_scale[(r0 + j) * 64 + h];
+          s.wq[slot][i] = v;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&s.qfull[slot], S::kQBytes);
+          tma_load_2d(s.q[slot], &tm_q, &s.qfull[slot], 0, r0 * 64);
+        } else {
+          mbar_arrive(&s.qfull[slot]);
+        }
+      }
+      const int npages_grp = div_up(cur.row_len(nr - 1), 64);
+      bool bad = false;
+      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        const int st = lt % kStages;
+        const int use = lt / kStages;
+        if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
+        if (lane == 0) {
+          const int pg0 = 2 * t, pg1 = 2 * t + 1;
+          const bool two = pg1 < npages_grp;
+          mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kPageKeyBytes + 256u));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !two) break;
+            int page = p.bt[static_cast<int64_t>(cur.req) * p.bt_stride + (h ? pg1 : pg0)];
+            if (page < 0 || page >= p.num_pages) {
+              raise_error(p.err, kErrBadPage);
+              page = 0;
+            }
+            tma_load_3d(s.keys[st] + h * kPageKeyBytes, &tm_k, &s.full[st], 0, 0, page);
+            bulk_load(&s.scales[st][h * 64],
+                      p.k_scale + static_cast<int64_t>(page) * p.s_page_stride, 256, &s.full[st]);
+          }
+        }
+        __syncwarp();
+      }
+      if (bad) break;
+      new_group = cur.next();
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer --
+    Cursor cur;
+    cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
+    int lt = 0;
+    bool new_group = true;
+    while (cur.valid() && !*abort) {
+      const int slot = cur.gcount & 1;
+      if (new_group && !mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+      const int tb = cur.tile_begin(), te = cur.tile_end();
+      bool bad = false;
+      for (int t = tb; t < te; ++t, ++lt) {
+        const int st = lt % kStages;
+        const int buf = lt & 1;
+        const int ub = lt >> 1;
+        if (!mbar_wait(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
+        if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(s.keys[st]);
+          const uint32_t b0 = smem_u32(s.q[slot]);
+          const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * N);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8f6f4(d, sw128_desc(a0 + 32 * k, 16, 1024), sw128_desc(b0 + 32 * k, 16, 1024),
+                       kIdesc, k > 0);
+          mma_commit(&s.empty[st]);
+          mma_commit(&s.tfull[buf]);
+        }
+        __syncwarp();
+      }
+      if (bad) break;
+      new_group = cur.next();
+      if (new_group && lane == 0) mma_commit(&s.qempty[slot]);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue --
+    const int wg = (warp - 2) >> 2;  // which accumulator this warpgroup drains
+    const int quad = warp & 3;       // TMEM lane quadrant of this warp
+    const int row_in_tile = quad * 32 + lane;
+    Cursor cur;
+    cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
+    int lt = 0;
+    while (cur.valid() && !*abort) {
+      const int slot = cur.gcount & 1;
+      bool waited_q = false;
+      const int r0 = cur.row0();
+      const int nr = cur.nrows();
+      bool bad = false;
+      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        if ((lt & 1) != wg) continue;
+        if (!waited_q) {
+          if (!mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
+          waited_q = true;
+        }
+        const int st = lt % kStages;
+        if (!mbar_wait(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
+        tc_fence_after();
+        const float sc = s.scales[st][row_in_tile];
+        const int tok = t * kTileTokens + row_in_tile;
+        const uint32_t taddr = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(wg * N);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float v[64];
+          tmem_ld64_sync(taddr + j * 64, v);
+          float acc = 0.f;
+          const float* wj = s.wq[slot] + j * 64;
+#pragma unroll
+          for (int h = 0; h < 64; ++h) acc = fmaf(wj[h], fmaxf(v[h], 0.f), acc);
+          if (j < nr && tok < cur.row_len(j))
+            p.logits[static_cast<int64_t>(r0 + j) * p.ld + tok] = acc * sc;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s.tempty[wg]);
+          mbar_arrive(&s.empty[st]);
+        }
+      }
+      if (bad) break;
+      const bool left = cur.next();
+      if (left && lane == 0) mbar_arrive(&s.qempty[slot]);
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(s.tmem_base, kTmemCols);
+  }
+}
+
+template <int G>
+cudaError_t launch_g(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                     const CUtensorMap& tk, const CUtensorMap& tq) {
+  const size_t smem = sizeof(Smem<G>) + 1024;
+  auto fn = indexer_kernel<G>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  KParams p;
+  p.q_scale = a.q_scale;
+  p.w = a.w;
+  p.k_scale = a.k_scale;
+  p.s_page_stride = a.s_page_stride;
+  p.num_pages = a.num_pages;
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.ctx_len = a.ctx_len;
+  p.num_req = a.num_req;
+  p.next_n = a.next_n;
+  p.logits = a.logits;
+  p.ld = a.ld;
+  p.err = dev.err_word;
+  fn<<<dev.sm_count, kThreads, smem, stream>>>(tk, tq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                           char* msg, size_t msg_len) {
+  if (a.num_req > kMaxReq) {
+    snprintf(msg, msg_len, "dsa_indexer_logits: num_req %d exceeds %d", a.num_req, kMaxReq);
+    return cudaErrorInvalidValue;
+  }
+  const int G = a.next_n >= 4 ? 4 : a.next_n;
+  CUtensorMap tk, tq;
+  {
+    // keys: [num_pages][64 tokens][128 bytes], page stride k_page_stride
+    const uint64_t dims[3] = {128, 64, static_cast<uint64_t>(a.num_pages)};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(a.k_page_stride)};
+    const uint32_t box[3] = {128, 64, 1};
+    if (!encode_tensor_map(&tk, 0, 3, const_cast<uint8_t*>(a.k_cache), dims, strides, box, true,
+                           msg, msg_len))
+      return cudaErrorInvalidValue;
+  }
+  {
+    // q: [R*64 rows][128 bytes]; one box = the N rows of a row group
+    const uint64_t rows = static_cast<uint64_t>(a.num_req) * a.next_n * 64;
+    const uint64_t dims[2] = {128, rows};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(64 * G)};
+    if (!encode_tensor_map(&tq, 0, 2, const_cast<uint8_t*>(a.q), dims, strides, box, true, msg,
+                           msg_len))
+      return cudaErrorInvalidValue;
+  }
+  switch (G) {
+    case 1: return launch_g<1>(a, dev, stream, tk, tq);
+    case 2: return launch_g<2>(a, dev, stream, tk, tq);
+    case 3: return launch_g<3>(a, dev, stream, tk, tq);
+    default: return launch_g<4>(a, dev, stream, tk, tq);
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,126 @@
+// Host-side launch interfaces between the C-ABI translation unit (dsa_api.cu)
+// and the kernel translation units.  Arguments are validated by the caller.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dsa {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  size_t smem_optin = 0;
+  uint32_t* err_word = nullptr;  // device address of this device's error word
+};
+
+// Fills `info` for the current device.
+cudaError_t current_device_info(DeviceInfo* info);
+
+// Encodes a CUtensorMap through the driver entry point (no libcuda link).
+// dtype: 0 = uint8, 1 = bf16.  Returns false (and a message) on failure.
+bool encode_tensor_map(void* map_out, int dtype, int rank, void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128,
+                       char* msg, size_t msg_len);
+
+struct IndexerArgs {
+  const uint8_t* q;
+  const float* q_scale;
+  const float* w;
+  const uint8_t* k_cache;
+  int64_t k_page_stride;
+  const uint8_t* k_scale;
+  int64_t s_page_stride;
+  int num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* ctx_len;
+  int num_req;
+  int next_n;
+  float* logits;
+  int64_t ld;
+};
+
+cudaError_t launch_indexer(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                           char* msg, size_t msg_len);
+
+struct TopkArgs {
+  const float* logits;
+  int64_t ld;
+  const int32_t* row_len;
+  int R;
+  int k;
+  const int32_t* col_blocks;
+  int nb;
+  int block_size;
+  int32_t* out;
+  int force_path;
+};
+
+cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+struct MlaArgs {
+  const uint16_t* q;
+  const uint16_t* kv;
+  int64_t kv_page_stride;
+  int num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int num_req;
+  int next_n;
+  const int32_t* idx;
+  int k;
+  float sm_scale;
+  uint16_t* out;
+  float* lse;
+  void* ws;
+  size_t ws_bytes;
+};
+
+size_t mla_workspace_size(int R, int k);
+cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+struct CandExpandArgs {
+  const int32_t* cand;
+  int R;
+  int nb;
+  int bs;
+  const int32_t* ctx_len;
+  int next_n;
+  int32_t* sparse_indices;
+  int32_t* end;
+  void* schedule;
+};
+
+size_t candidate_schedule_size(int R);
+cudaError_t launch_candidate_expand(const CandExpandArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream);
+
+struct CandLogitsArgs {
+  const uint8_t* q;
+  const float* q_scale;
+  const float* w;
+  const uint8_t* k_fp4;
+  int64_t k_page_stride;
+  const uint8_t* k_sf;
+  int64_t sf_page_stride;
+  int num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int num_req;
+  int next_n;
+  const int32_t* sparse_indices;
+  int nb;
+  int bs;
+  const int32_t* end;
+  const void* schedule;
+  float* logits;
+  int64_t ld;
+};
+
+cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream, char* msg, size_t msg_len);
+
+}  // namespace dsa

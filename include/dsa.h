@@ -1,0 +1,233 @@
+/*
+ * dsa.h -- C ABI of the DeepSeek Sparse Attention (DSA) decode hot path for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The path (Eq. (1) and Eq. (2) of "Feature Request: DeepSeek V3.2-Exp
+ * support", llama.cpp issue 16331, section "1. Architecture"):
+ *
+ *   1. lightning-indexer logits over a paged FP8 key cache  dsa_indexer_logits
+ *   2. exact per-row top-k of the logits                    dsa_topk
+ *   3. sparse MLA attention over the selected latents       dsa_sparse_mla_decode
+ *
+ * and the two-level candidate-block indexer of the vLLM "sparse_indexer"
+ * backend page (consumer layers score only the candidate blocks):
+ *
+ *   a. candidate expansion, once per step                   dsa_candidate_expand
+ *   b. candidate (sparse MQA) logits over MXFP4 keys        dsa_candidate_logits
+ *   c. top-k over the candidate columns, mapped to tokens   dsa_topk (col_blocks)
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Pointers documented as "device" point to GPU memory of the current
+ *   device; the caller allocates, owns and frees every buffer.  The library
+ *   allocates no memory per call: scratch comes from a caller-provided
+ *   workspace whose size the matching *_size query returns.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *   only enqueues work and returns; nothing is synchronised.
+ * - Every argument is validated on the host before anything is enqueued; an
+ *   unsupported shape or a bad argument returns an error and enqueues nothing.
+ *   There is no fallback path.  dsa_last_error() gives a message.
+ * - Device-side checks (block-table entries outside the cache, selected
+ *   indices outside a row, a wait that ran out) never trap: the kernel skips
+ *   the access, records a bit in a per-device error word and finishes.
+ *   dsa_get_device_error() reads (and optionally clears) that word.
+ * - Query rows are flattened per request: row r = b * next_n + j (j = 0 ..
+ *   next_n-1) is the j-th of the next_n consecutive query positions of
+ *   request b.  It sees L_r = ctx_len[b] - (next_n - 1 - j) cached tokens
+ *   (the cache already holds all next_n positions; a query sees itself).
+ * - Caches are paged with 64-token pages: token t of request b lives in page
+ *   block_table[b * bt_stride + t / 64], slot t % 64.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned buffer, ... */
+  DSA_ERR_UNSUPPORTED = 2, /* a shape or device this library does not implement */
+  DSA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the query said */
+  DSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (message has the code) */
+  DSA_ERR_DEVICE = 5       /* the device error word is set (dsa_get_device_error) */
+} dsa_status;
+
+/* Bits of the device error word. */
+#define DSA_DEVERR_TIMEOUT 0x1u   /* a bounded wait inside a kernel ran out */
+#define DSA_DEVERR_BAD_PAGE 0x2u  /* block-table entry outside [0, num_pages) */
+#define DSA_DEVERR_BAD_INDEX 0x4u /* selected index outside [0, L_r), or row_len > ld */
+#define DSA_DEVERR_CAPACITY 0x8u  /* cutoff estimate missed; the exact full-row path ran */
+
+/* Fixed problem sizes of the path (the indexer of Eq. (1) and the MLA of
+ * Eq. (2) as the DeepSeek V3.2 pages size them). */
+#define DSA_PAGE_TOKENS 64
+#define DSA_INDEX_HEADS 64 /* H^I */
+#define DSA_INDEX_DIM 128  /* d^I */
+#define DSA_MLA_HEADS 128
+#define DSA_MLA_DQK 576 /* 512 latent + 64 rope */
+#define DSA_MLA_DV 512
+#define DSA_MAX_TOPK 8192
+
+/* Version of this ABI (major*100 + minor). */
+int dsa_version(void);
+
+/* Message of the last failing call made by this host thread ("" if none). */
+const char* dsa_last_error(void);
+
+/* Reads the device error word of the current device after synchronising
+ * `stream`; clears it when `clear` != 0.  Returns DSA_OK (and *bits) or
+ * DSA_ERR_CUDA. */
+dsa_status dsa_get_device_error(void* stream, uint32_t* bits, int clear);
+
+/* ------------------------------------------------------------------------
+ * dsa_indexer_logits -- lightning-indexer logits, Eq. (1):
+ *
+ *   logits[r, t] = s_t * sum_h w[r,h] * sq[r,h] * ReLU(q'[r,h] . k'_t),  t < L_r
+ *
+ * which is I_{t,s} of Eq. (1) with q = sq * q' (per-head FP8 scale) and
+ * k = s_t * k' (per-token FP8 scale; both scales are positive, so they leave
+ * the ReLU).  FP8 is e4m3 ("fn": no inf; 0x7F/0xFF are NaN and unsupported).
+ *
+ *   q_fp8      device [R, 64, 128] e4m3 codes, R = num_req * next_n.
+ *   q_scale    device [R, 64] f32, > 0.
+ *   weights    device [R, 64] f32 (w of Eq. (1); any sign).
+ *   k_cache    device; page p's 64 keys (128 e4m3 bytes each, slot-major) start
+ *              at k_cache + p * k_page_stride bytes.  16-byte aligned, stride % 16 == 0.
+ *   k_scale    device; page p's 64 f32 per-token scales start at
+ *              k_scale + p * s_page_stride bytes.  16-byte aligned, stride % 16 == 0.
+ *              (The canonical page is 8448 bytes: keys, then scales.)
+ *   num_pages  pages in the cache (block-table entries must be < num_pages).
+ *   block_table device [num_req, bt_stride] int32; only the first ceil(L/64)
+ *              entries of a request are read.
+ *   ctx_len    device [num_req] int32 (>= 0).  num_req <= 4096.
+ *   next_n     query rows per request (1 = plain decode, 2 = MTP; a prefill
+ *              chunk of n queries is next_n = n).  1 <= next_n <= 65536.
+ *   logits     device [R, ld] f32; for each row only t < L_r is written.
+ *              ld >= max L_r, ld % 4 == 0, 16-byte aligned.
+ * Work: one TMA-fed tcgen05 (kind::f8f6f4) contraction per 128-token tile with
+ * the ReLU, head weighting and key scale fused into the TMEM epilogue.
+ * ---------------------------------------------------------------------- */
+dsa_status dsa_indexer_logits(const uint8_t* q_fp8, const float* q_scale, const float* weights,
+                              const uint8_t* k_cache, int64_t k_page_stride,
+                              const uint8_t* k_scale, int64_t s_page_stride, int num_pages,
+                              const int32_t* block_table, int64_t bt_stride,
+                              const int32_t* ctx_len, int num_req, int next_n, float* logits,
+                              int64_t ld, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_topk -- exact fine-grained token selection (the Top-k of Eq. (2)).
+ *
+ * For each row r: the k largest logits[r, c], c < row_len[r], as column
+ * indices in any order; a row with row_len <= k returns all its columns
+ * followed by -1.  Ties are broken towards the lower column, so the selected
+ * set equals the first k of a stable sort by score descending.  -0.0 == +0.0.
+ * NaN logits are unsupported.
+ *
+ * Long rows (row_len >= 65536 for k >= 1024, >= 98304 for k < 1024) take the
+ * cutoff path described for vLLM's persistent top-k: estimate a cutoff from a
+ * sample, compact the survivors into shared memory in one pass over the row,
+ * finish with an exact radix selection on them (redoing the row with the
+ * full-row radix if the estimate missed).  Shorter rows take the full-row
+ * radix select.  `force_path`: 0 = that rule, 1 = always full-row, 2 = always
+ * cutoff (for tests; the selected set is the same).
+ *
+ *   logits     device [R, ld] f32; ld % 4 == 0, 16-byte aligned.
+ *   row_len    device [R] int32 (0 <= row_len <= ld).
+ *   col_blocks NULL, or device [R, nb] int32: then column c is reported as token
+ *              col_blocks[r, c / block_size] * block_size + c % block_size
+ *              (the candidate path's sparse column -> token map).
+ *   out_idx    device [R, k] int32.
+ *   1 <= k <= DSA_MAX_TOPK.
+ * ---------------------------------------------------------------------- */
+dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
+                    const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
+                    int force_path, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_sparse_mla_decode -- sparse MLA attention, Eq. (2):
+ *
+ *   for head g of row r:  z_j = sm_scale * q[r,g,:] . c_{idx[r,j]}   (576-d)
+ *                         out[r,g,:] = sum_j softmax(z)_j c_{idx[r,j]}[0:512]
+ *                         lse[r,g]   = log sum_j exp(z_j)           (natural log)
+ *
+ * over the valid selected tokens only (idx = -1 is skipped; a row with none
+ * gives out = 0, lse = -inf).  Token positions are logical positions of the
+ * row's request (row r belongs to request r / next_n) and go through the block
+ * table.  bf16 inputs, f32 accumulation and softmax, bf16 output.
+ *
+ *   q         device [R, 128, 576] bf16.
+ *   kv_cache  device; page p = [64, 576] bf16 at kv_cache + p * kv_page_stride
+ *             bytes (16-byte aligned, stride % 16 == 0).
+ *   idx       device [R, k] int32, 1 <= k <= DSA_MAX_TOPK.
+ *   out       device [R, 128, 512] bf16.   lse  device [R, 128] f32 (may be NULL).
+ *   workspace device, dsa_sparse_mla_workspace_size(R, k) bytes (split-K
+ *             partial results; may be NULL when that size is 0).
+ * ---------------------------------------------------------------------- */
+size_t dsa_sparse_mla_workspace_size(int R, int k);
+
+dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache,
+                                 int64_t kv_page_stride, int num_pages,
+                                 const int32_t* block_table, int64_t bt_stride, int num_req,
+                                 int next_n, const int32_t* idx, int k, float sm_scale,
+                                 uint16_t* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_candidate_expand -- the once-per-step candidate expansion shared by all
+ * consumer indexer layers (vLLM sparse_indexer: sparse_indices, end and the
+ * kernel schedule are filled by the first consumer layer and reused).
+ *
+ *   cand           device [R, nb] int32 candidate block ids published by the
+ *                  source layer (distinct; ids >= ceil(L/bs) mark padding).
+ *   sparse_indices device [R, nb] int32 out: the ids sorted ascending.
+ *   end            device [R] int32 out: valid sparse columns of the row, i.e.
+ *                  #{c < nb*bs : 0 <= tok(c) < L_r}, tok(c) =
+ *                  sparse_indices[r, c/bs]*bs + c%bs.  (Sorted ascending, the
+ *                  valid columns are a prefix.)
+ *   schedule       device, dsa_candidate_schedule_size(R) bytes out: the work
+ *                  schedule dsa_candidate_logits reads.
+ *   block_size     candidate_block_size; must equal the 64-token page.
+ *   nb <= 4096.
+ * ---------------------------------------------------------------------- */
+size_t dsa_candidate_schedule_size(int R);
+
+dsa_status dsa_candidate_expand(const int32_t* cand, int R, int nb, int block_size,
+                                const int32_t* ctx_len, int next_n, int32_t* sparse_indices,
+                                int32_t* end, void* schedule, size_t schedule_bytes,
+                                void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_candidate_logits -- candidate (sparse MQA) logits over MXFP4 keys:
+ *
+ *   logits[r, c] = sum_h w[r,h] * sq[r,h] * ReLU(q'[r,h] . k_tok(c)),  c < end[r]
+ *
+ * with k the MXFP4-dequantised key: e2m1 elements (element 2i in the low
+ * nibble of byte i) times a UE8M0 scale 2^(e-127) per 32 elements.
+ *
+ *   k_fp4     device; page p's 64 keys (64 packed bytes each) at
+ *             k_fp4 + p * k_page_stride bytes.
+ *   k_sf      device; page p's 64 x 4 UE8M0 bytes (byte g of slot i scales
+ *             elements 32g..32g+31) at k_sf + p * sf_page_stride bytes.
+ *             (The canonical page is 4352 bytes: packed keys, then scales.)
+ *   sparse_indices, end, schedule: as written by dsa_candidate_expand.
+ *   logits    device [R, ld] f32, ld >= nb * block_size, ld % 4 == 0; only
+ *             c < end[r] is written.
+ * ---------------------------------------------------------------------- */
+dsa_status dsa_candidate_logits(const uint8_t* q_fp8, const float* q_scale, const float* weights,
+                                const uint8_t* k_fp4, int64_t k_page_stride, const uint8_t* k_sf,
+                                int64_t sf_page_stride, int num_pages,
+                                const int32_t* block_table, int64_t bt_stride, int num_req,
+                                int next_n, const int32_t* sparse_indices, int nb,
+                                int block_size, const int32_t* end, const void* schedule,
+                                size_t schedule_bytes, float* logits, int64_t ld, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */
