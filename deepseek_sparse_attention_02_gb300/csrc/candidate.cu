@@ -1,0 +1,491 @@
+// Two-level candidate-block indexer (the vLLM "sparse_indexer" backend page:
+// candidate consumer layers score only the candidate blocks published by the
+// source layer; the first consumer of a step fills sparse_indices, end and the
+// kernel schedule, later consumers reuse them; keys are MXFP4 with UE8M0
+// scales at granularity 32).
+//
+// candidate_expand: one CTA per row sorts its block ids (bitonic sort in
+// shared memory), counts the valid sparse columns (end) and writes the row's
+// work-chunk count; a one-CTA scan turns the counts into the schedule (an
+// exclusive prefix over rows) that candidate_logits walks.
+//
+// candidate_logits: the indexer pipeline of indexer.cu over candidate
+// columns.  A tile is 128 sparse columns = two candidate blocks = two
+// 64-token pages, fetched by cp.async.bulk (4096 packed bytes + 256 scale
+// bytes each).  The owning epilogue warpgroup expands e2m1 -> e4m3 (exact: every
+// e2m1 value is an e4m3 value) into a 128B-swizzled [128 x 128] tile with two
+// byte-permute lookups per 4 elements.  The MMA warp then issues one
+// kind::f8f6f4 MMA per 32-element scale group (K = 32) into four TMEM
+// accumulators, so the epilogue applies the UE8M0 scales exactly:
+//   logit = sum_h w'_h * ReLU(sum_g 2^(e_g - 127) * D_g[h]).
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kStages = 6;
+constexpr int kTileCols = 128;
+constexpr int kChunkTiles = 4;
+constexpr uint32_t kPackedPage = 64 * 64;  // 4096
+constexpr uint32_t kSfPage = 64 * 4;       // 256
+
+__device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------- expansion --
+
+__global__ void __launch_bounds__(256) candidate_expand_kernel(CandExpandArgs a, uint32_t* err) {
+  __shared__ int ids[4096];
+  __shared__ int red[8];
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  int n2 = 1;
+  while (n2 < a.nb) n2 <<= 1;
+  const int32_t* src = a.cand + static_cast<int64_t>(r) * a.nb;
+  for (int i = tid; i < n2; i += 256) ids[i] = i < a.nb ? src[i] : 0x7fffffff;
+  __syncthreads();
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n2 / 2; i += 256) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const int x = ids[lo], y = ids[hi];
+        if ((x > y) == asc) {
+          ids[lo] = y;
+          ids[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  const int req = r / a.next_n;
+  const int j = r % a.next_n;
+  const int64_t L = static_cast<int64_t>(a.ctx_len[req]) - (a.next_n - 1 - j);
+  int cnt = 0;
+  for (int i = tid; i < a.nb; i += 256) {
+    const int b = ids[i];
+    a.sparse_indices[static_cast<int64_t>(r) * a.nb + i] = b;
+    if (b < 0) {
+      raise_error(err, kErrBadIndex);
+      continue;
+    }
+    const int64_t v = L - static_cast<int64_t>(b) * a.bs;
+    cnt += static_cast<int>(v <= 0 ? 0 : (v >= a.bs ? a.bs : v));
+  }
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((tid & 31) == 0) red[tid >> 5] = cnt;
+  __syncthreads();
+  if (tid == 0) {
+    int tot = 0;
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    a.end[r] = tot;
+    int32_t* sched = static_cast<int32_t*>(a.schedule);
+    sched[r + 1] = div_up(div_up(tot, kTileCols), kChunkTiles);
+  }
+}
+
+// In-place exclusive prefix of sched[1..R] (sched[0] = 0) by one CTA.
+__global__ void __launch_bounds__(1024) schedule_scan_kernel(int32_t* sched, int R) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) {
+    carry = 0;
+    sched[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < R; base += 1024) {
+    const int i = base + tid;
+    int v = i < R ? sched[i + 1] : 0;
+    int incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      int s = warp_sums[lane];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += t;
+      }
+      warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int before = (w > 0 ? warp_sums[w - 1] : 0) + carry;
+    if (i < R) sched[i + 1] = before + incl;
+    __syncthreads();
+    if (tid == 1023) carry = before + incl;
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- logits --
+
+struct CParams {
+  const float* q_scale;
+  const float* w;
+  const uint8_t* k_fp4;
+  int64_t k_page_stride;
+  const uint8_t* k_sf;
+  int64_t sf_page_stride;
+  int num_pages;
+  const int32_t* bt;
+  int64_t bt_stride;
+  int next_n;
+  int R;
+  const int32_t* sparse_indices;
+  int nb;
+  const int32_t* end;
+  const int32_t* sched;  // [R+1] exclusive chunk prefix
+  float* logits;
+  int64_t ld;
+  uint32_t* err;
+};
+
+// Walks the chunks [c, c_end) of this CTA; one row per group.
+struct RowCursor {
+  const int32_t* sched;
+  const int32_t* end;
+  int R;
+  int c, c_end, row, tiles, gchunk, nchunk, gcount;
+  __device__ void enter() {
+    tiles = div_up(end[row], kTileCols);
+    nchunk = div_up(tiles, kChunkTiles);
+  }
+  __device__ void init(const int32_t* sc, const int32_t* en, int nrows, int c0, int c1) {
+    sched = sc;
+    end = en;
+    R = nrows;
+    c = c0;
+    c_end = c1;
+    gcount = 0;
+    if (c >= c_end) return;
+    int lo = 0, hi = R;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sched[mid] <= c) lo = mid; else hi = mid;
+    }
+    row = lo;
+    while (sched[row + 1] <= c) ++row;
+    enter();
+    gchunk = c - sched[row];
+  }
+  __device__ bool valid() const { return c < c_end; }
+  __device__ int tile_begin() const { return gchunk * kChunkTiles; }
+  __device__ int tile_end() const { return min(tiles, gchunk * kChunkTiles + kChunkTiles); }
+  __device__ bool next() {
+    ++c;
+    if (c >= c_end) return true;
+    if (++gchunk < nchunk) return false;
+    gchunk = 0;
+    do {
+      ++row;
+    } while (row < R && sched[row + 1] == sched[row]);
+    if (row < R) enter();
+    ++gcount;
+    return true;
+  }
+};
+
+struct CSmem {
+  uint8_t a[2][128 * 128];           // converted e4m3 key tiles, K-major SW128
+  uint8_t q[2][64 * 128];            // q of the row, K-major SW128
+  uint8_t raw[kStages][2 * kPackedPage];
+  uint8_t sf[kStages][2 * kSfPage];
+  float wq[2][64];
+  uint64_t full[kStages], empty[kStages];
+  uint64_t qfull[2], qempty[2];
+  uint64_t afull[2], tfull[2], tempty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// e2m1 magnitude code -> e4m3 byte: {0, 0.5, 1, 1.5 | 2, 3, 4, 6}
+constexpr uint32_t kLutLo = 0x3C383000u;
+constexpr uint32_t kLutHi = 0x4C484440u;
+
+// Four e2m1 nibbles (low 16 bits of x) -> four e4m3 bytes.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t x) {
+  const uint32_t mag = __byte_perm(kLutLo, kLutHi, x & 0x7777u);
+  const uint32_t neg = __byte_perm(0u, 0xffffffffu, (x >> 1) & 0x4444u);
+  return mag | (neg & 0x80808080u);
+}
+
+__device__ __forceinline__ float ue8m0_to_float(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    candidate_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const CParams p) {
+  constexpr uint32_t kTmemCols = 512;  // two buffers of four [128 x 64] accumulators
+  constexpr uint32_t kIdesc = make_idesc(0, 0, 128, 64, false, false);
+  extern __shared__ uint8_t smem_raw[];
+  CSmem& s = *reinterpret_cast<CSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+    s.abort = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.qfull[i], 32);
+      mbar_init(&s.qempty[i], 1 + 8);
+      mbar_init(&s.afull[i], 128);
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int total = p.sched[p.R];
+  const int c0 = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
+  const int c1 = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
+  volatile int* abort = &s.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    RowCursor cur;
+    cur.init(p.sched, p.end, p.R, c0, c1);
+    if (lane == 0) tma_prefetch_desc(&tm_q);
+    int lt = 0;
+    bool new_group = true;
+    while (cur.valid() && !*abort) {
+      const int r = cur.row;
+      const int req = r / p.next_n;
+      if (new_group) {
+        const int slot = cur.gcount & 1;
+        const int use = cur.gcount >> 1;
+        if (use > 0 && !mbar_wait(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
+        for (int i = lane; i < 64; i += 32) s.wq[slot][i] = p.w[r * 64 + i] * p.q_scale[r * 64 + i];
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&s.qfull[slot], 64 * 128);
+          tma_load_2d(s.q[slot], &tm_q, &s.qfull[slot], 0, r * 64);
+        } else {
+          mbar_arrive(&s.qfull[slot]);
+        }
+      }
+      const int endr = p.end[r];
+      bool bad = false;
+      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        const int st = lt % kStages;
+        const int use = lt / kStages;
+        if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
+        if (lane == 0) {
+          const bool two = (2 * t + 1) * 64 < endr;
+          mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kPackedPage + kSfPage));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1 && !two) break;
+            const int blk = p.sparse_indices[static_cast<int64_t>(r) * p.nb + 2 * t + h];
+            int page = -1;
+            if (blk >= 0 && blk < p.bt_stride)
+              page = p.bt[static_cast<int64_t>(req) * p.bt_stride + blk];
+            if (page < 0 || page >= p.num_pages) {
+              raise_error(p.err, kErrBadPage);
+              page = 0;
+            }
+            bulk_load(s.raw[st] + h * kPackedPage,
+                      p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride, kPackedPage,
+                      &s.full[st]);
+            bulk_load(s.sf[st] + h * kSfPage,
+                      p.k_sf + static_cast<int64_t>(page) * p.sf_page_stride, kSfPage,
+                      &s.full[st]);
+          }
+        }
+        __syncwarp();
+      }
+      if (bad) break;
+      new_group = cur.next();
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer --
+    RowCursor cur;
+    cur.init(p.sched, p.end, p.R, c0, c1);
+    int lt = 0;
+    bool new_group = true;
+    while (cur.valid() && !*abort) {
+      const int slot = cur.gcount & 1;
+      if (new_group && !mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+      bool bad = false;
+      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        const int buf = lt & 1;
+        const int ub = lt >> 1;
+        if (!mbar_wait(&s.afull[buf], ub & 1, p.err, abort)) { bad = true; break; }
+        if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(s.a[buf]);
+          const uint32_t b0 = smem_u32(s.q[slot]);
+          const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * 256);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            mma_f8f6f4(d + 64 * g, sw128_desc(a0 + 32 * g, 16, 1024),
+                       sw128_desc(b0 + 32 * g, 16, 1024), kIdesc, 0);
+          mma_commit(&s.tfull[buf]);
+        }
+        __syncwarp();
+      }
+      if (bad) break;
+      new_group = cur.next();
+      if (new_group && lane == 0) mma_commit(&s.qempty[slot]);
+      __syncwarp();
+    }
+  } else {
+    // -------------------------------------- convert + epilogue warpgroups --
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int tr = quad * 32 + lane;  // token row of the tile == TMEM lane
+    RowCursor cur;
+    cur.init(p.sched, p.end, p.R, c0, c1);
+    int lt = 0;
+    while (cur.valid() && !*abort) {
+      const int slot = cur.gcount & 1;
+      const int r = cur.row;
+      const int endr = p.end[r];
+      bool waited_q = false, bad = false;
+      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        if ((lt & 1) != wg) continue;
+        const int st = lt % kStages;
+        if (!mbar_wait(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
+        // expand this thread's token row: 64 packed bytes -> 128 e4m3 bytes
+        const uint8_t* src = s.raw[st] + (tr >> 6) * kPackedPage + (tr & 63) * 64;
+        uint8_t* dst = s.a[wg];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * j);
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            o[2 * u] = e2m1x4_to_e4m3(in[u]);
+            o[2 * u + 1] = e2m1x4_to_e4m3(in[u] >> 16);
+          }
+          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * j)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * j + 1)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        const uint32_t sfw =
+            *reinterpret_cast<const uint32_t*>(s.sf[st] + (tr >> 6) * kSfPage + (tr & 63) * 4);
+        fence_proxy_async_smem();
+        mbar_arrive(&s.afull[wg]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[st]);
+        float sc[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) sc[g] = ue8m0_to_float((sfw >> (8 * g)) & 0xffu);
+        if (!waited_q) {
+          if (!mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
+          waited_q = true;
+        }
+        if (!mbar_wait(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
+        tc_fence_after();
+        const uint32_t taddr = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(wg * 256);
+        float acc = 0.f;
+#pragma unroll
+        for (int hc = 0; hc < 4; ++hc) {
+          float d0[16], d1[16], d2[16], d3[16];
+          tmem_ld16_sync(taddr + 0 * 64 + 16 * hc, d0);
+          tmem_ld16_sync(taddr + 1 * 64 + 16 * hc, d1);
+          tmem_ld16_sync(taddr + 2 * 64 + 16 * hc, d2);
+          tmem_ld16_sync(taddr + 3 * 64 + 16 * hc, d3);
+          const float* wh = s.wq[slot] + 16 * hc;
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const float x = fmaf(sc[3], d3[h], fmaf(sc[2], d2[h], fmaf(sc[1], d1[h], sc[0] * d0[h])));
+            acc = fmaf(wh[h], fmaxf(x, 0.f), acc);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.tempty[wg]);
+        const int col = t * kTileCols + tr;
+        if (col < endr) p.logits[static_cast<int64_t>(r) * p.ld + col] = acc;
+      }
+      if (bad) break;
+      const bool left = cur.next();
+      if (left && lane == 0) mbar_arrive(&s.qempty[slot]);
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(s.tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t candidate_schedule_size(int R) {
+  return (static_cast<size_t>(R) + 1 + 3) / 4 * 16;
+}
+
+cudaError_t launch_candidate_expand(const CandExpandArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream) {
+  candidate_expand_kernel<<<a.R, 256, 0, stream>>>(a, dev.err_word);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  schedule_scan_kernel<<<1, 1024, 0, stream>>>(static_cast<int32_t*>(a.schedule), a.R);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream, char* msg, size_t msg_len) {
+  const int R = a.num_req * a.next_n;
+  CUtensorMap tq;
+  {
+    const uint64_t dims[2] = {128, static_cast<uint64_t>(R) * 64};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {128, 64};
+    if (!encode_tensor_map(&tq, 0, 2, const_cast<uint8_t*>(a.q), dims, strides, box, true, msg,
+                           msg_len))
+      return cudaErrorInvalidValue;
+  }
+  CParams p;
+  p.q_scale = a.q_scale;
+  p.w = a.w;
+  p.k_fp4 = a.k_fp4;
+  p.k_page_stride = a.k_page_stride;
+  p.k_sf = a.k_sf;
+  p.sf_page_stride = a.sf_page_stride;
+  p.num_pages = a.num_pages;
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.next_n = a.next_n;
+  p.R = R;
+  p.sparse_indices = a.sparse_indices;
+  p.nb = a.nb;
+  p.end = a.end;
+  p.sched = static_cast<const int32_t*>(a.schedule);
+  p.logits = a.logits;
+  p.ld = a.ld;
+  p.err = dev.err_word;
+  const size_t smem = sizeof(CSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(candidate_logits_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  candidate_logits_kernel<<<dev.sm_count, kThreads, smem, stream>>>(tq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

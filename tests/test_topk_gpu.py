@@ -1,0 +1,75 @@
+"""Parity of dsa_topk with the oracle's full-sort selection on the same fp32
+logits (exact: the selected sets must be identical, ties to the lower
+column)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_check import gpu_topk, np_
+
+pytestmark = pytest.mark.gpu
+
+
+def sets_equal(sel, logits, L, k):
+    ref = oracle.topk(np_(logits).astype(np.float64), np_(L), k)
+    s = np_(sel)
+    for i in range(s.shape[0]):
+        assert sorted(s[i].tolist()) == sorted(ref[i].tolist()), f"row {i}"
+
+
+@pytest.mark.parametrize("force", [0, 1, 2])
+def test_topk_random_rows(force):
+    g = torch.Generator(device="cuda").manual_seed(1)
+    L = torch.tensor([0, 1, 2047, 2048, 2049, 4099, 8192, 33333, 65536, 70001, 131072],
+                     dtype=torch.int32, device="cuda")
+    ld = 131072
+    logits = torch.randn(len(L), ld, generator=g, device="cuda")
+    sel = gpu_topk(logits, ld, L, 2048, force_path=force)
+    sets_equal(sel, logits, L, 2048)
+
+
+@pytest.mark.parametrize("force", [1, 2])
+def test_topk_heavy_ties(force):
+    g = torch.Generator(device="cuda").manual_seed(2)
+    L = torch.tensor([5000, 70000, 100000], dtype=torch.int32, device="cuda")
+    ld = 100000
+    logits = torch.randint(-6, 6, (3, ld), generator=g, device="cuda").float()
+    logits[0, ::3] = -0.0
+    logits[0, 1::3] = 0.0
+    sel = gpu_topk(logits, ld, L, 1000, force_path=force)
+    sets_equal(sel, logits, L, 1000)
+
+
+def test_topk_all_equal_takes_exact_fallback():
+    from deepseek_sparse_attention_02_gb300 import dsa
+    dsa.dsa_get_device_error(clear=True)
+    L = torch.tensor([90000], dtype=torch.int32, device="cuda")
+    logits = torch.full((1, 90000), 0.25, device="cuda")
+    sel = gpu_topk(logits, 90000, L, 2048, force_path=2)
+    assert sorted(np_(sel)[0].tolist()) == list(range(2048))
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error(clear=True) == dsa.DEVERR_CAPACITY
+
+
+def test_topk_small_k_and_odd_sizes():
+    g = torch.Generator(device="cuda").manual_seed(3)
+    L = torch.tensor([3, 10, 17, 1000], dtype=torch.int32, device="cuda")
+    logits = torch.randn(4, 1000, generator=g, device="cuda")
+    for k in (1, 7, 16):
+        sel = gpu_topk(logits, 1000, L, k)
+        sets_equal(sel, logits, L, k)
+
+
+def test_topk_column_map():
+    g = torch.Generator(device="cuda").manual_seed(4)
+    R, nb, bs = 3, 40, 64
+    cols = nb * bs
+    logits = torch.randn(R, cols, generator=g, device="cuda")
+    L = torch.tensor([cols, cols - 17, 100], dtype=torch.int32, device="cuda")
+    blocks = torch.stack([torch.randperm(500, generator=torch.Generator().manual_seed(r))[:nb]
+                          for r in range(R)]).to(torch.int32).cuda()
+    sel = gpu_topk(logits, cols, L, 256, col_blocks=blocks, bs=bs)
+    ref = oracle.topk(np_(logits).astype(np.float64), np_(L), 256, col_blocks=np_(blocks), bs=bs)
+    for i in range(R):
+        assert sorted(np_(sel)[i].tolist()) == sorted(ref[i].tolist())
