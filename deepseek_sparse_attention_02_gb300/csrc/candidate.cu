@@ -154,11 +154,14 @@ struct RowCursor {
   const int32_t* end;
   int R;
   int c, c_end, row, tiles, gchunk, nchunk, gcount;
+  int max_cols;
   __device__ void enter() {
-    tiles = div_up(end[row], kTileCols);
+    tiles = div_up(min(end[row], max_cols), kTileCols);
     nchunk = div_up(tiles, kChunkTiles);
   }
-  __device__ void init(const int32_t* sc, const int32_t* en, int nrows, int c0, int c1) {
+  __device__ void init(const int32_t* sc, const int32_t* en, int nrows, int c0, int c1,
+                       int cols) {
+    max_cols = cols;
     sched = sc;
     end = en;
     R = nrows;
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     RowCursor cur;
-    cur.init(p.sched, p.end, p.R, c0, c1);
+    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
     if (lane == 0) tma_prefetch_desc(&tm_q);
     int lt = 0;
     bool new_group = true;
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&s.qfull[slot]);
         }
       }
-      const int endr = p.end[r];
+      const int endr = min(p.end[r], p.nb * 64);
       bool bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
         const int st = lt % kStages;
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer --
     RowCursor cur;
-    cur.init(p.sched, p.end, p.R, c0, c1);
+    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
     int lt = 0;
     bool new_group = true;
     while (cur.valid() && !*abort) {
@@ -352,12 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int tr = quad * 32 + lane;  // token row of the tile == TMEM lane
     RowCursor cur;
-    cur.init(p.sched, p.end, p.R, c0, c1);
+    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
     int lt = 0;
     while (cur.valid() && !*abort) {
       const int slot = cur.gcount & 1;
       const int r = cur.row;
-      const int endr = p.end[r];
+      const int endr = min(p.end[r], p.nb * 64);
       bool waited_q = false, bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
         if ((lt & 1) != wg) continue;
@@ -479,7 +482,8 @@ cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& d
   p.logits = a.logits;
   p.ld = a.ld;
   p.err = dev.err_word;
-  const size_t smem = sizeof(CSmem) + 1024;
+  // at least 120 KB so that one CTA (holding all 512 TMEM columns) runs per SM
+  const size_t smem = sizeof(CSmem) + 1024 > 120 * 1024 ? sizeof(CSmem) + 1024 : 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(candidate_logits_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

@@ -295,7 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (h == 1 && !two) break;
-            int page = p.bt[static_cast<int64_t>(cur.req) * p.bt_stride + (h ? pg1 : pg0)];
+            const int pg = h ? pg1 : pg0;
+            int page = pg < p.bt_stride ? p.bt[static_cast<int64_t>(cur.req) * p.bt_stride + pg] : -1;
             if (page < 0 || page >= p.num_pages) {
               raise_error(p.err, kErrBadPage);
               page = 0;
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* wj = s.wq[slot] + j * 64;
 #pragma unroll
           for (int h = 0; h < 64; ++h) acc = fmaf(wj[h], fmaxf(v[h], 0.f), acc);
-          if (j < nr && tok < cur.row_len(j))
+          if (j < nr && tok < cur.row_len(j) && tok < p.ld)
             p.logits[static_cast<int64_t>(r0 + j) * p.ld + tok] = acc * sc;
         }
         tc_fence_before();

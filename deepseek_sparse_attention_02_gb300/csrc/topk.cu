@@ -253,6 +253,10 @@ __device__ Sel cluster_select(const Src& src, uint32_t need, int max_depth, TkSm
 
 __device__ __forceinline__ int32_t map_col(const TkParams& p, int row, uint32_t col) {
   if (!p.col_blocks) return static_cast<int32_t>(col);
+  if (col / static_cast<uint32_t>(p.bs) >= static_cast<uint32_t>(p.nb)) {
+    raise_error(p.err, kErrBadIndex);
+    return -1;
+  }
   const int64_t blk = p.col_blocks[static_cast<int64_t>(row) * p.nb + col / p.bs];
   return static_cast<int32_t>(blk * p.bs + col % p.bs);
 }
