@@ -1,0 +1,471 @@
+#!/usr/bin/env python3
+"""Benchmark of the DSA decode hot path on one GB300 (or N replicas).
+
+Headline step (the 128K-context MTP decode workload): 32 requests x 131072
+cached tokens, next_n = 2 (64 query rows), 64 index heads x 128 FP8 keys in
+64-token pages behind a shuffled block table, then
+  1. dsa_indexer_logits   (Eq. (1) over all 8.4 M (row, key) pairs)
+  2. dsa_topk             (exact top-2048 per row; cutoff path)
+  3. dsa_sparse_mla_decode (128 heads x 576-d bf16 latents of the selected tokens)
+The candidate-block path (64 x 196608 ctx, 512 candidate blocks, MXFP4 keys,
+one expansion + 4 consumer layers of candidate logits + top-k) is timed in the
+same run and reported under "candidate_path".
+
+value = indexer keys scored (row, key pairs) per second of the whole step.
+All inputs are seeded synthetic data generated on the device; the key cache
+(553 MB) and the latent cache (4.8 GB) are larger than L2, so no flush is
+needed between steps.
+
+--impl reference times the fp64 CPU oracle (the reference arm) on bounded
+samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexer keys scored/s + HBM GB/s at 128K decode; top-k rows/s; sparse-attn tok/s"
+WORKLOAD = ("128K MTP decode: 32 requests x 131072 ctx, next_n=2 (64 rows), FP8 indexer "
+            "64x128 over 64-token shuffled pages, exact top-2048, sparse MLA 128 heads x "
+            "576-d bf16 latents")
+TOPK = 2048
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        try:
+            rows = [l.strip().split(", ") for l in open(self.path) if l.strip()]
+        except Exception:
+            return out
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                continue
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                   "reasons": sorted(reasons), "samples": len(sm)}
+        return out
+
+
+# ------------------------------------------------------------------ our arm --
+
+def build_decode(device, seed=0):
+    import torch
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case = W.make_indexer_case([131072] * 32, next_n=2, seed=seed, device=device)
+    R = case.rows
+    L = W.row_lengths(case.layout.ctx_len, 2).to(torch.int32)
+    ld = 131072
+    mla = W.make_mla_case(R, case.layout.num_pages, seed=seed, device=device)
+    st = dict(case=case, R=R, L=L, ld=ld, mla=mla)
+    st["logits"] = torch.empty((R, ld), device=device)
+    st["idx"] = torch.empty((R, TOPK), dtype=torch.int32, device=device)
+    st["out"] = torch.empty((R, W.MLA_HEADS, W.MLA_DV), dtype=torch.bfloat16, device=device)
+    st["lse"] = torch.empty((R, W.MLA_HEADS), device=device)
+    from deepseek_sparse_attention_02_gb300 import dsa
+    wsb = dsa.dsa_sparse_mla_workspace_size(R, TOPK)
+    st["ws"] = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
+    st["wsb"] = wsb
+    return st
+
+
+def decode_kernels(st):
+    """The three launches of one decode step, as callables."""
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case, R, ld = st["case"], st["R"], st["ld"]
+    c = case.cache
+    lay = case.layout
+
+    def indexer():
+        dsa.dsa_indexer_logits(case.q, case.q_scale, case.w, c, W.FP8_PAGE_BYTES,
+                               c.data_ptr() + W.FP8_KEY_BYTES, W.FP8_PAGE_BYTES, lay.num_pages,
+                               lay.block_table, lay.ctx_len, len(lay.ctx_len), 2, st["logits"], ld)
+
+    def topk():
+        dsa.dsa_topk(st["logits"], ld, st["L"], R, TOPK, st["idx"])
+
+    def mla():
+        m = st["mla"]
+        dsa.dsa_sparse_mla_decode(m.q, m.kv, 64 * 576 * 2, lay.num_pages, lay.block_table,
+                                  len(lay.ctx_len), 2, st["idx"], TOPK, m.scale, st["out"],
+                                  st["lse"], st["ws"], st["wsb"])
+
+    return [("indexer", indexer), ("topk", topk), ("sparse_mla", mla)]
+
+
+def build_candidate(device, seed=3):
+    import torch
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    ctx = [196608] * 64
+    layers = [W.make_indexer_case(ctx, next_n=1, seed=seed + i, device=device, fmt="mxfp4")
+              for i in range(4)]
+    cand = W.make_candidates(ctx, 1, 64, 512, seed=seed, device=device)
+    R, nb = cand.shape
+    nbytes = dsa.dsa_candidate_schedule_size(R)
+    st = dict(layers=layers, cand=cand, R=R, nb=nb, sched_bytes=nbytes,
+              si=torch.empty_like(cand), end=torch.empty(R, dtype=torch.int32, device=device),
+              sched=torch.zeros(nbytes // 4, dtype=torch.int32, device=device),
+              logits=torch.empty((R, nb * 64), device=device),
+              idx=torch.empty((4, R, TOPK), dtype=torch.int32, device=device))
+    return st
+
+
+def candidate_kernels(st):
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    R, nb = st["R"], st["nb"]
+    ld = nb * 64
+    lay0 = st["layers"][0].layout
+    ks = [("expand", lambda: dsa.dsa_candidate_expand(st["cand"], R, nb, 64, lay0.ctx_len, 1,
+                                                      st["si"], st["end"], st["sched"],
+                                                      st["sched_bytes"]))]
+    for i, case in enumerate(st["layers"]):
+        def logits(case=case):
+            c = case.cache
+            dsa.dsa_candidate_logits(case.q, case.q_scale, case.w, c, W.FP4_PAGE_BYTES,
+                                     c.data_ptr() + W.FP4_KEY_BYTES, W.FP4_PAGE_BYTES,
+                                     case.layout.num_pages, case.layout.block_table, R, 1,
+                                     st["si"], nb, 64, st["end"], st["sched"], st["sched_bytes"],
+                                     st["logits"], ld)
+
+        def topk(i=i):
+            dsa.dsa_topk(st["logits"], ld, st["end"], R, TOPK, st["idx"][i], col_blocks=st["si"],
+                         nb=nb, block_size=64)
+        ks.append((f"cand_logits_{i}", logits))
+        ks.append((f"cand_topk_{i}", topk))
+    return ks
+
+
+def time_kernels(kernels, steps, warmup, stream):
+    """Runs `steps` timed passes; returns (total ms, {name: mean ms per launch})."""
+    import torch
+    for _ in range(warmup):
+        for _, fn in kernels:
+            fn()
+    torch.cuda.synchronize()
+    n = len(kernels)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(steps):
+        ev[s][0].record(stream)
+        for j, (_, fn) in enumerate(kernels):
+            fn()
+            ev[s][j + 1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    per = {}
+    for j, (name, _) in enumerate(kernels):
+        per[name] = sum(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(steps)) / steps
+    return start.elapsed_time(end), per
+
+
+def e2e_decode(st, steps, warmup, stream):
+    """Same step through the public API with per-step host inputs (pinned) copied in
+    and the step's outputs copied out inside the timed region."""
+    import torch
+    case, mla = st["case"], st["mla"]
+    dev_inputs = [case.q, case.q_scale, case.w, case.layout.block_table, case.layout.ctx_len,
+                  mla.q]
+    host_inputs = [t.cpu().pin_memory() for t in dev_inputs]
+    dev_outputs = [st["out"], st["lse"], st["idx"]]
+    host_outputs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_outputs]
+    kernels = decode_kernels(st)
+
+    def step():
+        for h, d in zip(host_inputs, dev_inputs):
+            d.copy_(h, non_blocking=True)
+        for _, fn in kernels:
+            fn()
+        for h, d in zip(host_outputs, dev_outputs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    d2h = sum(t.numel() * t.element_size() for t in host_outputs)
+    return ms, h2d, d2h
+
+
+def cpu_baseline_sample(rows=16, threads=None):
+    """The oracle on a bounded sample of the headline workload: `rows` of the 64
+    query rows (indexer over their 131072 keys, full-sort top-2048 and the
+    sparse attention of those rows).  Returns (keys/s, cores, seconds, desc)."""
+    import numpy as np
+    import torch
+    import oracle
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    nreq = max(1, (rows + 1) // 2)
+    case = W.make_indexer_case([131072] * nreq, next_n=2, seed=0, device="cpu")
+    mla = W.make_mla_case(case.rows, case.layout.num_pages, seed=0, device="cpu")
+    sel_rows = np.arange(min(rows, case.rows), dtype=np.int32)
+    th = threads or oracle.hardware_threads()
+    cache = case.cache.numpy().reshape(-1)
+    t0 = time.perf_counter()
+    ref, _ = oracle.indexer_logits(case.q.numpy(), case.q_scale.numpy(), case.w.numpy(), cache,
+                                   W.FP8_PAGE_BYTES, cache[W.FP8_KEY_BYTES:], W.FP8_PAGE_BYTES,
+                                   64, case.layout.block_table.numpy(),
+                                   case.layout.ctx_len.numpy(), 2, rows=sel_rows, nthreads=th)
+    L = oracle.row_lengths(case.layout.ctx_len.numpy(), 2)[sel_rows]
+    idx_sel = oracle.topk(ref, L, TOPK, nthreads=th)
+    idx_full = np.full((case.rows, TOPK), -1, np.int32)
+    idx_full[sel_rows] = idx_sel
+    oracle.sparse_mla(W.bf16_bits(mla.q).numpy().view(np.uint16),
+                      W.bf16_bits(mla.kv).numpy().view(np.uint16), 64 * 576, 64,
+                      case.layout.block_table.numpy(), 2, idx_full, mla.scale, rows=sel_rows,
+                      nthreads=th)
+    dt = time.perf_counter() - t0
+    keys = float(L.sum())
+    desc = (f"{len(sel_rows)} of the 64 query rows (131071/131072 keys each): oracle indexer, "
+            f"full-sort top-2048 and sparse MLA of those rows; keys/s = their keys / time")
+    return keys / dt, th, dt, desc
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def reduce_max(pg, value: float, device):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg, device):
+    if pg is not None:
+        if device.type == "cuda":
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def run_ours(args):
+    import torch
+    world, rank, local, pg = dist_setup()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import __graft_entry__ as g
+    g.build()
+    from deepseek_sparse_attention_02_gb300 import dsa
+    stream = torch.cuda.current_stream()
+    st = build_decode(device)
+    kernels = decode_kernels(st)
+    cst = build_candidate(device)
+    ckernels = candidate_kernels(cst)
+    torch.cuda.synchronize()
+
+    barrier(pg, device)
+    with ClockSampler(local) as clocks:
+        total_ms, per = time_kernels(kernels, args.steps, args.warmup, stream)
+        c_total_ms, c_per = time_kernels(ckernels, args.steps, args.warmup, stream)
+    barrier(pg, device)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0, "device error word set during the benchmark"
+    ms_step = total_ms / args.steps
+    ms_step_max = reduce_max(pg, ms_step, device)
+
+    keys_per_step = float(st["L"].sum().item())
+    value = world * keys_per_step / (ms_step_max * 1e-3)
+    hbm, bf16_tf, peak_src = peaks()
+    # dominant kernel: the indexer (HBM-bound): 128 B key + 4 B scale per cached
+    # token read, 4 B logit per (row, key) written
+    tokens = 32 * 131072
+    alg_bytes = tokens * 132 + keys_per_step * 4
+    t_idx = per["indexer"] * 1e-3
+    achieved = alg_bytes / t_idx / 1e9
+    e2e_ms, h2d, d2h = e2e_decode(st, args.steps, args.warmup, stream)
+    e2e_ms = reduce_max(pg, e2e_ms, device)
+    R = st["R"]
+    # candidate path numbers
+    cand_keys = float(cst["end"].sum().item()) * 4
+    c_ms = c_total_ms / args.steps
+    c_log = statistics.mean(c_per[f"cand_logits_{i}"] for i in range(4))
+    c_bytes = float(cst["end"].sum().item()) * 68 + float(cst["end"].sum().item()) * 4
+    ctk = statistics.mean(c_per[f"cand_topk_{i}"] for i in range(4))
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "keys/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8-e4m3 indexer (f32 accumulate), f32 top-k, bf16 MLA (f32 accumulate)",
+        "data": "synthetic (seeded, generated on device)",
+        "config": {"workload": WORKLOAD, "global_batch": 64 * world, "seq_len": 131072,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (553.6 MB key cache, 4.8 GB latent cache); no flush"},
+        "breakdown_ms": {k: round(v, 4) for k, v in per.items()},
+        "indexer": {"keys_per_s": keys_per_step / t_idx, "hbm_gbs": achieved,
+                    "unique_keys_per_s": tokens / t_idx},
+        "topk": {"rows_per_s": R / (per["topk"] * 1e-3),
+                 "logit_gbs": keys_per_step * 4 / (per["topk"] * 1e-3) / 1e9},
+        "sparse_mla": {"attended_tok_per_s": R * TOPK / (per["sparse_mla"] * 1e-3),
+                       "gather_gbs": R * TOPK * 1152 / (per["sparse_mla"] * 1e-3) / 1e9,
+                       "tflops": R * 2 * 128 * TOPK * (576 + 512) / (per["sparse_mla"] * 1e-3) / 1e12},
+        "candidate_path": {"workload": "64 requests x 196608 ctx, 512 candidate blocks of 64, "
+                                       "MXFP4 keys, 1 expansion + 4 consumer layers (logits + top-2048)",
+                           "ms_per_step": c_ms,
+                           "breakdown_ms": {k: round(v, 4) for k, v in c_per.items()},
+                           "candidate_keys_per_s": cand_keys / (c_ms * 1e-3),
+                           "logits_hbm_gbs": c_bytes / (c_log * 1e-3) / 1e9,
+                           "topk_rows_per_s": cst["R"] / (ctk * 1e-3)},
+        "roofline": {"kernel": "dsa_indexer_logits", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": peak_src,
+                     "alg_bytes_per_launch": alg_bytes},
+        "gpu_launches": args.steps * (len(kernels) + (1 if st["wsb"] > 0 else 0)) +
+                        args.steps * (len(ckernels) + 1),
+        "e2e": {"value": world * keys_per_step / (e2e_ms * 1e-3), "unit": "keys/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks.summary(),
+    }
+    traffic = os.environ.get("DSA_INDEXER_TRAFFIC_BYTES")
+    if traffic:
+        line["roofline"]["traffic"] = float(traffic)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, dt, desc = cpu_baseline_sample(rows=args.cpu_rows)
+        line["cpu_baseline"] = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    vals, dts = [], []
+    desc, cores = "", 1
+    for _ in range(args.warmup):
+        cpu_baseline_sample(rows=args.cpu_rows)
+    for _ in range(args.steps):
+        v, cores, dt, desc = cpu_baseline_sample(rows=args.cpu_rows)
+        vals.append(v)
+        dts.append(dt)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(dts),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "global_batch": 64, "seq_len": 131072,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "keys/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
