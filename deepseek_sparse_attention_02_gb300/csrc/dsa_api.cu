@@ -32,7 +32,7 @@ dsa_status ok() {
   return DSA_OK;
 }
 
-// One error word per device: the library's only device-resident state.
+// One error word per device.
 __device__ uint32_t g_err_word;
 
 constexpr int kMaxDevices = 64;
@@ -327,6 +327,46 @@ dsa_status dsa_candidate_logits(const uint8_t* q_fp8, const float* q_scale, cons
   cudaError_t e =
       launch_candidate_logits(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
   if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
+  return cuda_status(e, fn);
+}
+
+
+size_t dsa_sparse_mla_static_scratch_bytes(void) { return mla_static_scratch_bytes(); }
+
+dsa_status dsa_sparse_mla_decode_static(const uint16_t* q, const uint16_t* kv_cache,
+                                        int64_t kv_page_stride, int num_pages,
+                                        const int32_t* block_table, int64_t bt_stride,
+                                        int num_req, int next_n, const int32_t* idx, int k,
+                                        float sm_scale, uint16_t* out, float* lse,
+                                        void* stream) {
+  const char* fn = "dsa_sparse_mla_decode_static";
+  if (!q || !kv_cache || !block_table || !idx || !out)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (num_req < 0 || next_n < 1 || num_pages < 1 || bt_stride < 1 || k < 1 ||
+      k > DSA_MAX_TOPK || !(sm_scale > 0.f))
+    return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes or scale", fn);
+  if (kv_page_stride < 64 * 576 * 2 || kv_page_stride % 16 || !aligned16(kv_cache) ||
+      !aligned16(q) || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: kv page stride must be >= 73728 and a multiple of 16; q, kv and out "
+                "16-byte aligned",
+                fn);
+  const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
+  if (R64 > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
+  if (R64 == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  MlaArgs a{q,   kv_cache, kv_page_stride, num_pages, block_table, bt_stride, num_req, next_n,
+            idx, k,        sm_scale,       out,       lse,         nullptr,   0};
+  size_t need = 0;
+  const cudaError_t e =
+      launch_sparse_mla_static(a, dev, static_cast<cudaStream_t>(stream), &need);
+  if (e == cudaErrorMemoryAllocation)
+    return fail(DSA_ERR_UNSUPPORTED,
+                "%s: this batch needs %zu bytes of split-K scratch but the static scratch holds "
+                "%zu; call dsa_sparse_mla_decode with a workspace instead",
+                fn, need, mla_static_scratch_bytes());
   return cuda_status(e, fn);
 }
 

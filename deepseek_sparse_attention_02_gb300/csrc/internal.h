@@ -82,6 +82,13 @@ struct MlaArgs {
 size_t mla_workspace_size(int R, int k);
 cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
+// No-allocation variant: split-K scratch from a static device array.
+// Returns cudaErrorMemoryAllocation (and *need) when the batch needs more
+// scratch than the array holds.
+size_t mla_static_scratch_bytes();
+cudaError_t launch_sparse_mla_static(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                                     size_t* need);
+
 struct CandExpandArgs {
   const int32_t* cand;
   int R;

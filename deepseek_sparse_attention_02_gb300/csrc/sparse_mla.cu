@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -487,6 +488,57 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   if (e != cudaSuccess || ns == 1) return e;
   mla_combine_kernel<<<dim3(R, 2), 256, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+
+// ------------------------------------------------ no-allocation variant --
+// Split-K scratch for callers that cannot allocate device memory.  The array
+// lives in the module for as long as the library is loaded, once per device.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(24) << 20;  // 24 MiB
+static __device__ __align__(256) unsigned char g_mla_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxScratchDevices] = {};
+
+// Device address of this device's copy of the array.  In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, taken once per device with that device current.
+cudaError_t static_scratch_address(int device, void** out) {
+  if (device < 0 || device >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[device]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_mla_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[device] = ptr;
+  }
+  *out = g_scratch_ptr[device];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t mla_static_scratch_bytes() { return kStaticScratchBytes; }
+
+cudaError_t launch_sparse_mla_static(const MlaArgs& a_in, const DeviceInfo& dev,
+                                     cudaStream_t stream, size_t* need) {
+  const int R = a_in.num_req * a_in.next_n;
+  *need = mla_workspace_size(R, a_in.k);
+  if (*need > kStaticScratchBytes) return cudaErrorMemoryAllocation;
+  MlaArgs a = a_in;
+  a.ws = nullptr;
+  a.ws_bytes = 0;
+  if (*need > 0) {
+    void* ptr = nullptr;
+    const cudaError_t e = static_scratch_address(dev.device, &ptr);
+    if (e != cudaSuccess) return e;
+    a.ws = ptr;
+    a.ws_bytes = kStaticScratchBytes;
+  }
+  return launch_sparse_mla(a, dev, stream);
 }
 
 }  // namespace dsa

@@ -42,6 +42,9 @@ _SIGS = {
     "dsa_sparse_mla_workspace_size": ([_I, _I], _SZ),
     "dsa_sparse_mla_decode": ([_P, _P, _I64, _I, _P, _I64, _I, _I, _P, _I, _F, _P, _P, _P, _SZ,
                                _P], _I),
+    "dsa_sparse_mla_static_scratch_bytes": ([], _SZ),
+    "dsa_sparse_mla_decode_static": ([_P, _P, _I64, _I, _P, _I64, _I, _I, _P, _I, _F, _P, _P, _P],
+                                     _I),
     "dsa_candidate_schedule_size": ([_I], _SZ),
     "dsa_candidate_expand": ([_P, _I, _I, _I, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "dsa_candidate_logits": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _I, _I, _P, _I, _I,
@@ -136,6 +139,22 @@ def dsa_sparse_mla_decode(q, kv_cache, kv_page_stride, num_pages, block_table, n
                                       _ptr(block_table), bt_stride, num_req, next_n, _ptr(idx), k,
                                       float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                       workspace_bytes, _stream(stream)))
+
+
+def dsa_sparse_mla_static_scratch_bytes() -> int:
+    return int(_lib.dsa_sparse_mla_static_scratch_bytes())
+
+
+def dsa_sparse_mla_decode_static(q, kv_cache, kv_page_stride, num_pages, block_table, num_req,
+                                 next_n, idx, k, sm_scale, out, lse=None, stream=None):
+    """dsa_sparse_mla_decode without a workspace, for callers that cannot
+    allocate device memory; its split-K scratch is a static array inside the
+    library (see include/dsa.h)."""
+    bt_stride = block_table.shape[1]
+    _check(_lib.dsa_sparse_mla_decode_static(_ptr(q), _ptr(kv_cache), kv_page_stride, num_pages,
+                                             _ptr(block_table), bt_stride, num_req, next_n,
+                                             _ptr(idx), k, float(sm_scale), _ptr(out), _ptr(lse),
+                                             _stream(stream)))
 
 
 def dsa_candidate_schedule_size(R: int) -> int:

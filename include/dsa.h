@@ -178,6 +178,42 @@ dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache,
                                  size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsa_sparse_mla_decode_static -- dsa_sparse_mla_decode for callers that
+ * cannot allocate device memory.  (No counterpart in the paper: this is an
+ * interface convenience of this library, not part of the method.)
+ *
+ * Who needs it: code that is not allowed to call cudaMalloc -- for example a
+ * plug-in running inside a host program that owns all device memory and
+ * hands out no allocator, or a latency-critical loop that cannot afford the
+ * implicit device synchronisation a cudaMalloc may cause -- and so cannot
+ * provide the workspace of dsa_sparse_mla_decode.
+ *
+ * Same arguments and results as dsa_sparse_mla_decode, without the workspace:
+ * the split-K partial results go to a scratch array compiled into the library
+ * (dsa_sparse_mla_static_scratch_bytes() = 24 MiB, held on every GPU that
+ * loads the library until the process exits).  The work split is the same as
+ * dsa_sparse_mla_decode's, so the outputs are the same.  A batch whose
+ * partials would not fit returns DSA_ERR_UNSUPPORTED with the size it needs
+ * (use dsa_sparse_mla_decode then).  Nothing is allocated, by this call or by
+ * the library.
+ *
+ * The first call on a device looks up that device's scratch address
+ * (cudaGetSymbolAddress, once per device, with the device current); make that
+ * first call before any stream capture.  All calls on a device share the one
+ * scratch array and it keeps the previous call's contents (no part of it has
+ * to start at zero: each call writes every value it reads back); calls that
+ * overlap on the GPU -- on two streams, or from two host threads -- race on
+ * it, so serialise them.
+ * ---------------------------------------------------------------------- */
+size_t dsa_sparse_mla_static_scratch_bytes(void);
+
+dsa_status dsa_sparse_mla_decode_static(const uint16_t* q, const uint16_t* kv_cache,
+                                        int64_t kv_page_stride, int num_pages,
+                                        const int32_t* block_table, int64_t bt_stride,
+                                        int num_req, int next_n, const int32_t* idx, int k,
+                                        float sm_scale, uint16_t* out, float* lse, void* stream);
+
+/* ------------------------------------------------------------------------
  * dsa_candidate_expand -- the once-per-step candidate expansion shared by all
  * consumer indexer layers (vLLM sparse_indexer: sparse_indices, end and the
  * kernel schedule are filled by the first consumer layer and reused).
