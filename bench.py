@@ -108,10 +108,10 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm --
 
-def build_decode(device, seed=0):
+def build_decode(device, seed=0, requests=32):
     import torch
     from deepseek_sparse_attention_02_gb300 import workloads as W
-    case = W.make_indexer_case([131072] * 32, next_n=2, seed=seed, device=device)
+    case = W.make_indexer_case([131072] * requests, next_n=2, seed=seed, device=device)
     R = case.rows
     L = W.row_lengths(case.layout.ctx_len, 2).to(torch.int32)
     ld = 131072
@@ -330,16 +330,17 @@ def run_ours(args):
     g.build()
     from deepseek_sparse_attention_02_gb300 import dsa
     stream = torch.cuda.current_stream()
-    st = build_decode(device)
+    st = build_decode(device, requests=args.requests)
     kernels = decode_kernels(st)
-    cst = build_candidate(device)
-    ckernels = candidate_kernels(cst)
+    cst = None if args.no_candidate else build_candidate(device)
+    ckernels = [] if cst is None else candidate_kernels(cst)
     torch.cuda.synchronize()
 
     barrier(pg, device)
     with ClockSampler(local) as clocks:
         total_ms, per = time_kernels(kernels, args.steps, args.warmup, stream)
-        c_total_ms, c_per = time_kernels(ckernels, args.steps, args.warmup, stream)
+        if ckernels:
+            c_total_ms, c_per = time_kernels(ckernels, args.steps, args.warmup, stream)
     barrier(pg, device)
     torch.cuda.synchronize()
     assert dsa.dsa_get_device_error() == 0, "device error word set during the benchmark"
@@ -351,7 +352,7 @@ def run_ours(args):
     hbm, bf16_tf, peak_src = peaks()
     # dominant kernel: the indexer (HBM-bound): 128 B key + 4 B scale per cached
     # token read, 4 B logit per (row, key) written
-    tokens = 32 * 131072
+    tokens = args.requests * 131072
     alg_bytes = tokens * 132 + keys_per_step * 4
     t_idx = per["indexer"] * 1e-3
     achieved = alg_bytes / t_idx / 1e9
@@ -359,11 +360,20 @@ def run_ours(args):
     e2e_ms = reduce_max(pg, e2e_ms, device)
     R = st["R"]
     # candidate path numbers
-    cand_keys = float(cst["end"].sum().item()) * 4
-    c_ms = c_total_ms / args.steps
-    c_log = statistics.mean(c_per[f"cand_logits_{i}"] for i in range(4))
-    c_bytes = float(cst["end"].sum().item()) * 68 + float(cst["end"].sum().item()) * 4
-    ctk = statistics.mean(c_per[f"cand_topk_{i}"] for i in range(4))
+    cand = None
+    if cst is not None:
+        cand_keys = float(cst["end"].sum().item()) * 4
+        c_ms = c_total_ms / args.steps
+        c_log = statistics.mean(c_per[f"cand_logits_{i}"] for i in range(4))
+        c_bytes = float(cst["end"].sum().item()) * 68 + float(cst["end"].sum().item()) * 4
+        ctk = statistics.mean(c_per[f"cand_topk_{i}"] for i in range(4))
+        cand = {"workload": "64 requests x 196608 ctx, 512 candidate blocks of 64, "
+                            "MXFP4 keys, 1 expansion + 4 consumer layers (logits + top-2048)",
+                "ms_per_step": c_ms,
+                "breakdown_ms": {k: round(v, 4) for k, v in c_per.items()},
+                "candidate_keys_per_s": cand_keys / (c_ms * 1e-3),
+                "logits_hbm_gbs": c_bytes / (c_log * 1e-3) / 1e9,
+                "topk_rows_per_s": cst["R"] / (ctk * 1e-3)}
 
     line = {
         "metric": METRIC,
@@ -378,7 +388,10 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "fp8-e4m3 indexer (f32 accumulate), f32 top-k, bf16 MLA (f32 accumulate)",
         "data": "synthetic (seeded, generated on device)",
-        "config": {"workload": WORKLOAD, "global_batch": 64 * world, "seq_len": 131072,
+        "config": {"workload": WORKLOAD if args.requests == 32 else
+                   WORKLOAD.replace("32 requests", f"{args.requests} requests").replace(
+                       "(64 rows)", f"({2 * args.requests} rows)"),
+                   "global_batch": 2 * args.requests * world, "seq_len": 131072,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (553.6 MB key cache, 4.8 GB latent cache); no flush"},
         "breakdown_ms": {k: round(v, 4) for k, v in per.items()},
@@ -389,19 +402,13 @@ def run_ours(args):
         "sparse_mla": {"attended_tok_per_s": R * TOPK / (per["sparse_mla"] * 1e-3),
                        "gather_gbs": R * TOPK * 1152 / (per["sparse_mla"] * 1e-3) / 1e9,
                        "tflops": R * 2 * 128 * TOPK * (576 + 512) / (per["sparse_mla"] * 1e-3) / 1e12},
-        "candidate_path": {"workload": "64 requests x 196608 ctx, 512 candidate blocks of 64, "
-                                       "MXFP4 keys, 1 expansion + 4 consumer layers (logits + top-2048)",
-                           "ms_per_step": c_ms,
-                           "breakdown_ms": {k: round(v, 4) for k, v in c_per.items()},
-                           "candidate_keys_per_s": cand_keys / (c_ms * 1e-3),
-                           "logits_hbm_gbs": c_bytes / (c_log * 1e-3) / 1e9,
-                           "topk_rows_per_s": cst["R"] / (ctk * 1e-3)},
+        "candidate_path": cand,
         "roofline": {"kernel": "dsa_indexer_logits", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                      "peak_source": peak_src,
                      "alg_bytes_per_launch": alg_bytes},
         "gpu_launches": args.steps * (len(kernels) + (1 if st["wsb"] > 0 else 0)) +
-                        args.steps * (len(ckernels) + 1),
+                        (args.steps * (len(ckernels) + 1) if ckernels else 0),
         "e2e": {"value": world * keys_per_step / (e2e_ms * 1e-3), "unit": "keys/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
@@ -458,6 +465,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=32,
+                    help="decode requests (32 = the 128K workload; fewer for profiling)")
+    ap.add_argument("--no-candidate", action="store_true",
+                    help="skip the candidate-path leg (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

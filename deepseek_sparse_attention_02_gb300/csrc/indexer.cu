@@ -259,6 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_q);
     }
+    // Page ids of a chunk (at most 2 * kChunkTiles) are loaded by the lanes of
+    // this warp one chunk ahead, so no block-table load sits on the TMA issue path.
+    auto chunk_pages = [&](const Cursor& c) -> int {
+      if (!c.valid()) return -1;
+      const int npg = div_up(c.row_len(c.nrows() - 1), 64);
+      const int pg = 2 * c.tile_begin() + lane;
+      if (lane >= 2 * kChunkTiles || pg >= npg) return -1;
+      return pg < p.bt_stride ? p.bt[static_cast<int64_t>(c.req) * p.bt_stride + pg] : -2;
+    };
+    Cursor ahead = cur;
+    int pages_cur = chunk_pages(cur);
+    if (ahead.valid()) ahead.next();
+    int pages_next = chunk_pages(ahead);
     int lt = 0;  // local tile counter
     bool new_group = true;
     while (cur.valid() && !*abort) {
@@ -283,20 +296,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int npages_grp = div_up(cur.row_len(nr - 1), 64);
+      const int tb = cur.tile_begin();
       bool bad = false;
-      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+      for (int t = tb; t < cur.tile_end(); ++t, ++lt) {
         const int st = lt % kStages;
         const int use = lt / kStages;
         if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
+        const int pid0 = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb));
+        const int pid1 = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb) + 1);
         if (lane == 0) {
-          const int pg0 = 2 * t, pg1 = 2 * t + 1;
+          const int pg1 = 2 * t + 1;
           const bool two = pg1 < npages_grp;
           mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kPageKeyBytes + 256u));
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (h == 1 && !two) break;
-            const int pg = h ? pg1 : pg0;
-            int page = pg < p.bt_stride ? p.bt[static_cast<int64_t>(cur.req) * p.bt_stride + pg] : -1;
+            int page = h ? pid1 : pid0;
             if (page < 0 || page >= p.num_pages) {
               raise_error(p.err, kErrBadPage);
               page = 0;
@@ -310,6 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (bad) break;
       new_group = cur.next();
+      pages_cur = pages_next;
+      if (ahead.valid()) {
+        ahead.next();
+        pages_next = chunk_pages(ahead);
+      }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer --

@@ -198,32 +198,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kChunks; ++c) tma_load_2d(s.q[c], &tm_q, &s.q_full, 64 * c, row * kHeads);
     }
     const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
-    constexpr int kDepth = 3;  // chunks kept in flight per thread
+    // Token pointers: idx is read two tiles ahead and the block table one tile
+    // ahead, so neither load sits on the path that issues a tile's copies.
+    auto load_tok = [&](int i) -> int {
+      const int pos = s0 + i * kTile + gt;
+      return (gt < kTile && i < ntile && pos < s1) ? idx_row[pos] : -1;
+    };
+    auto load_page = [&](int tok) -> int {
+      if (tok < 0) return -1;
+      const int64_t pg_i = tok / 64;
+      return pg_i < p.bt_stride ? p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i] : -1;
+    };
+    auto make_ptr = [&](int tok, int page) -> const uint8_t* {
+      if (tok < 0) return nullptr;
+      if (page < 0 || page >= p.num_pages) {
+        raise_error(p.err, kErrBadIndex);
+        return nullptr;
+      }
+      return kvb + static_cast<int64_t>(page) * p.kv_page_stride +
+             static_cast<int64_t>(tok % 64) * (kDqk * 2);
+    };
+    int tok_a = load_tok(0);
+    int tok_b = load_tok(1);
+    if (gt < kTile) s.tokptr[0][gt] = make_ptr(tok_a, load_page(tok_a));
+    constexpr int kDepth = 4;  // chunks kept in flight per thread
     int issued = 0;            // chunks issued so far (global chunk counter)
     int signalled = 0;
     bool bad = false;
-    for (int i = 0; i < ntile && !bad; ++i) {
+    // Every gather thread passes exactly one named barrier per tile, even after
+    // an abort, so no thread can be left waiting on the barrier.
+    for (int i = 0; i < ntile; ++i) {
       const int tb = i & 1;
-      if (gt < kTile) {
-        const int pos = s0 + i * kTile + gt;
-        const uint8_t* ptr = nullptr;
-        if (pos < s1) {
-          const int tok = idx_row[pos];
-          if (tok >= 0) {
-            const int64_t pg_i = tok / 64;
-            int page = -1;
-            if (pg_i < p.bt_stride) page = p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i];
-            if (page >= 0 && page < p.num_pages) {
-              ptr = kvb + static_cast<int64_t>(page) * p.kv_page_stride +
-                    static_cast<int64_t>(tok % 64) * (kDqk * 2);
-            } else {
-              raise_error(p.err, kErrBadIndex);
-            }
-          }
-        }
-        s.tokptr[tb][gt] = ptr;
-      }
       named_bar_sync(1, kGather);
+      if (bad || *abort) {
+        bad = true;
+        continue;
+      }
+      int page_b = -1, tok_c = -1;
+      if (gt < kTile && i + 1 < ntile) {
+        page_b = load_page(tok_b);
+        tok_c = load_tok(i + 2);
+      }
       for (int qq = 0; qq < kChunks; ++qq) {
         const int g = i * kChunks + qq;
         const int slot = g % kRing;
@@ -249,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++signalled;
         }
       }
+      if (gt < kTile && i + 1 < ntile) {
+        s.tokptr[tb ^ 1][gt] = make_ptr(tok_b, page_b);
+        tok_b = tok_c;
+      }
     }
     cp_async_wait<0>();
     fence_proxy_async_smem();
@@ -264,7 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     float m_run = -INFINITY, l_run = 0.f;
     bool bad = false;
+    // validity of a tile's 64 selections: lane j of every warp reads entries j
+    // and 32 + j, the two ballots give the tile's mask (read one tile ahead)
+    auto load_sel = [&](int i, int off) -> int {
+      const int pos = s0 + i * kTile + off + lane;
+      return (i < ntile && pos < s1) ? idx_row[pos] : -1;
+    };
+    int sel_lo = load_sel(0, 0), sel_hi = load_sel(0, 32);
     for (int i = 0; i < ntile; ++i) {
+      const unsigned m_lo = __ballot_sync(0xffffffffu, sel_lo >= 0);
+      const unsigned m_hi = __ballot_sync(0xffffffffu, sel_hi >= 0);
+      sel_lo = load_sel(i + 1, 0);
+      sel_hi = load_sel(i + 1, 32);
       const int buf = i & 1;
       if (!mbar_wait(&s.s_full[buf], (i >> 1) & 1, p.err, abort)) { bad = true; break; }
       tc_fence_after();
@@ -273,24 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.s_empty[buf]);
-      // validity of the tile's tokens (same for every head)
-      const int base = s0 + i * kTile;
       float mt = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kTile; j += 4) {
-        int4 t4 = make_int4(-1, -1, -1, -1);
-        if (base + j + 3 < s1) {
-          t4 = *reinterpret_cast<const int4*>(idx_row + base + j);
-        } else {
-          if (base + j < s1) t4.x = idx_row[base + j];
-          if (base + j + 1 < s1) t4.y = idx_row[base + j + 1];
-          if (base + j + 2 < s1) t4.z = idx_row[base + j + 2];
-        }
-        x[j] = t4.x >= 0 ? x[j] * p.scale_log2 : -INFINITY;
-        x[j + 1] = t4.y >= 0 ? x[j + 1] * p.scale_log2 : -INFINITY;
-        x[j + 2] = t4.z >= 0 ? x[j + 2] * p.scale_log2 : -INFINITY;
-        x[j + 3] = t4.w >= 0 ? x[j + 3] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, fmaxf(fmaxf(x[j], x[j + 1]), fmaxf(x[j + 2], x[j + 3])));
+      for (int j = 0; j < kTile; ++j) {
+        const bool ok = ((j < 32 ? (m_lo >> j) : (m_hi >> (j - 32))) & 1u) != 0;
+        x[j] = ok ? x[j] * p.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, x[j]);
       }
       // PV(i-1) must be complete before P is overwritten or O rescaled
       if (i > 0 && !mbar_wait(&s.pv_done, (i - 1) & 1, p.err, abort)) { bad = true; break; }
