@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.qfull[i], 32);
       mbar_init(&s.qempty[i], 1 + 8);
-      mbar_init(&s.afull[i], 128);
+      mbar_init(&s.afull[i], 4);  // one arrival per converting warp
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], 4);
     }
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (new_group) {
         const int slot = cur.gcount & 1;
         const int use = cur.gcount >> 1;
-        if (use > 0 && !mbar_wait(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
+        if (use > 0 && !mbar_wait_warp(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
         for (int i = lane; i < 64; i += 32) s.wq[slot][i] = p.w[r * 64 + i] * p.q_scale[r * 64 + i];
         __syncwarp();
         if (lane == 0) {
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
         const int st = lt % kStages;
         const int use = lt / kStages;
-        if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
+        if (use > 0 && !mbar_wait_warp(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
         if (lane == 0) {
           const bool two = (2 * t + 1) * 64 < endr;
           mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kPackedPage + kSfPage));
@@ -324,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool new_group = true;
     while (cur.valid() && !*abort) {
       const int slot = cur.gcount & 1;
-      if (new_group && !mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+      if (new_group && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
       bool bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
         const int buf = lt & 1;
         const int ub = lt >> 1;
-        if (!mbar_wait(&s.afull[buf], ub & 1, p.err, abort)) { bad = true; break; }
-        if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
+        if (!mbar_wait_warp(&s.afull[buf], ub & 1, p.err, abort)) { bad = true; break; }
+        if (ub > 0 && !mbar_wait_warp(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(s.a[buf]);
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
         if ((lt & 1) != wg) continue;
         const int st = lt % kStages;
-        if (!mbar_wait(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
+        if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
         // expand this thread's token row: 64 packed bytes -> 128 e4m3 bytes
         const uint8_t* src = s.raw[st] + (tr >> 6) * kPackedPage + (tr & 63) * 64;
         uint8_t* dst = s.a[wg];
@@ -386,17 +386,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sfw =
             *reinterpret_cast<const uint32_t*>(s.sf[st] + (tr >> 6) * kSfPage + (tr & 63) * 4);
         fence_proxy_async_smem();
-        mbar_arrive(&s.afull[wg]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.empty[st]);
+        if (lane == 0) {
+          mbar_arrive(&s.afull[wg]);
+          mbar_arrive(&s.empty[st]);
+        }
         float sc[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) sc[g] = ue8m0_to_float((sfw >> (8 * g)) & 0xffu);
         if (!waited_q) {
-          if (!mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
+          if (!mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
           waited_q = true;
         }
-        if (!mbar_wait(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
+        if (!mbar_wait_warp(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
         const uint32_t taddr = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(wg * 256);
@@ -422,8 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (col < endr) p.logits[static_cast<int64_t>(r) * p.ld + col] = acc;
       }
       if (bad) break;
+      // A warp may walk through a group without processing any of its tiles (they
+      // went to the other warpgroup).  It still waits for that group's Q before it
+      // arrives on the slot's qempty, so its arrival cannot land in the phase of
+      // the group that used the slot two groups earlier.
+      if (!waited_q && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+      const int gslot = slot;
       const bool left = cur.next();
-      if (left && lane == 0) mbar_arrive(&s.qempty[slot]);
+      if (left && lane == 0) mbar_arrive(&s.qempty[gslot]);
       __syncwarp();
     }
   }

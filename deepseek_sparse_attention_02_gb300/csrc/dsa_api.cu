@@ -233,12 +233,14 @@ dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache,
   if (num_req < 0 || next_n < 1 || num_pages < 1 || bt_stride < 1 || k < 1 ||
       k > DSA_MAX_TOPK || !(sm_scale > 0.f))
     return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes or scale", fn);
-  if (kv_page_stride < 64 * 576 * 2 || kv_page_stride % 16 || !aligned16(kv_cache) ||
-      !aligned16(q) || !aligned16(out))
+  if (kv_page_stride != 64 * 576 * 2 || !aligned16(kv_cache) || !aligned16(q) ||
+      !aligned16(out))
     return fail(DSA_ERR_INVALID_ARG,
-                "%s: kv page stride must be >= 73728 and a multiple of 16; q, kv and out "
+                "%s: latent pages must be contiguous (kv_page_stride == 73728); q, kv and out "
                 "16-byte aligned",
                 fn);
+  if (static_cast<int64_t>(num_pages) * 64 > (1ll << 31) - 1)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: more than 2^31 cached latent rows", fn);
   const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
   if (R64 > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
   const int R = static_cast<int>(R64);
@@ -345,12 +347,14 @@ dsa_status dsa_sparse_mla_decode_static(const uint16_t* q, const uint16_t* kv_ca
   if (num_req < 0 || next_n < 1 || num_pages < 1 || bt_stride < 1 || k < 1 ||
       k > DSA_MAX_TOPK || !(sm_scale > 0.f))
     return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes or scale", fn);
-  if (kv_page_stride < 64 * 576 * 2 || kv_page_stride % 16 || !aligned16(kv_cache) ||
-      !aligned16(q) || !aligned16(out))
+  if (kv_page_stride != 64 * 576 * 2 || !aligned16(kv_cache) || !aligned16(q) ||
+      !aligned16(out))
     return fail(DSA_ERR_INVALID_ARG,
-                "%s: kv page stride must be >= 73728 and a multiple of 16; q, kv and out "
+                "%s: latent pages must be contiguous (kv_page_stride == 73728); q, kv and out "
                 "16-byte aligned",
                 fn);
+  if (static_cast<int64_t>(num_pages) * 64 > (1ll << 31) - 1)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: more than 2^31 cached latent rows", fn);
   const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
   if (R64 > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
   if (R64 == 0) return ok();

@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (new_group) {
         const int slot = cur.gcount & 1;
         const int use = cur.gcount >> 1;
-        if (use > 0 && !mbar_wait(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
+        if (use > 0 && !mbar_wait_warp(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
         for (int i = lane; i < N; i += 32) {
           const int j = i >> 6, h = i & 63;
           float v = 0.f;
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = tb; t < cur.tile_end(); ++t, ++lt) {
         const int st = lt % kStages;
         const int use = lt / kStages;
-        if (use > 0 && !mbar_wait(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
+        if (use > 0 && !mbar_wait_warp(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
         const int pid0 = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb));
         const int pid1 = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb) + 1);
         if (lane == 0) {
@@ -339,15 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool new_group = true;
     while (cur.valid() && !*abort) {
       const int slot = cur.gcount & 1;
-      if (new_group && !mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+      if (new_group && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
       const int tb = cur.tile_begin(), te = cur.tile_end();
       bool bad = false;
       for (int t = tb; t < te; ++t, ++lt) {
         const int st = lt % kStages;
         const int buf = lt & 1;
         const int ub = lt >> 1;
-        if (!mbar_wait(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
-        if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
+        if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
+        if (ub > 0 && !mbar_wait_warp(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(s.keys[st]);
@@ -384,11 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
         if ((lt & 1) != wg) continue;
         if (!waited_q) {
-          if (!mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
+          if (!mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
           waited_q = true;
         }
         const int st = lt % kStages;
-        if (!mbar_wait(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
+        if (!mbar_wait_warp(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
         const float sc = s.scales[st][row_in_tile];
         const int tok = t * kTileTokens + row_in_tile;
@@ -413,8 +413,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (bad) break;
+      // A warp may walk through a group without processing any of its tiles (they
+      // went to the other warpgroup).  It still waits for that group's Q before it
+      // arrives on the slot's qempty, so its arrival cannot land in the phase of
+      // the group that used the slot two groups earlier.
+      if (!waited_q && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+      const int gslot = slot;
       const bool left = cur.next();
-      if (left && lane == 0) mbar_arrive(&s.qempty[slot]);
+      if (left && lane == 0) mbar_arrive(&s.qempty[gslot]);
       __syncwarp();
     }
   }

@@ -3,21 +3,23 @@
 // over only the k selected latents c_s (576 = 512 latent + 64 rope elements;
 // the value is the first 512).
 //
-// Work unit = one CTA per (row, value half vh, split):
-//   * Q of the row (128 heads x 576 bf16, 147 KB) is loaded once by TMA into
-//     nine 128B-swizzled [128 x 64] K-chunks;
-//   * the split's selected tokens are taken 64 at a time; their latents are
-//     gathered by 16-byte cp.async into nine [64 tokens x 64] 128B-swizzled
-//     chunks that flow through an 8-slot ring (the chunks outside this CTA's
-//     value half first, so they free their slots early);
-//   * S = Q K^T (M = 128 heads, N = 64 tokens, K = 576) runs on tcgen05
-//     kind::f16 into TMEM;
-//   * the softmax warpgroup (one thread per head / TMEM lane) masks invalid
-//     tokens, keeps a running max (rescaling O in TMEM only when the max grows
-//     by more than 2^8), writes P = exp2(S*scale*log2e - m) as bf16 into a
-//     swizzled smem tile;
-//   * O[128 x 256] += P V_half runs on tcgen05 with V read MN-major straight
-//     from the gathered chunks.
+// Work unit = one CTA per (row, value half vh, split); 128 selected tokens per
+// tile.
+//   warp 0     gather producer: Q of the row once (TMA, nine 128B-swizzled
+//              [128 x 64] K-chunks); then per tile the nine [128 tokens x 64]
+//              K-chunks of the selected latents, and one tile later the four
+//              value chunks of this CTA's half again (an L2 hit), through a
+//              5-slot ring of 16 KB, by TMA tile::gather4 (each lane fetches 4
+//              rows; a skipped selection reads an out-of-range row = zeros);
+//   warp 1     tcgen05 issuer, in the order S(0), S(1), PV(0), S(2), PV(1), ...:
+//              S = Q K^T (kind::f16, M = 128 heads, N = 128 tokens, K = 576)
+//              into one of two TMEM tiles; O[128 x 256] += P V_half with P read
+//              from TMEM and V read MN-major from the ring (N = 256 when the
+//              four value chunks are contiguous in the ring, else two MMAs);
+//   warps 4-7  softmax (one thread per head / TMEM lane): mask skipped
+//              selections, running max with lazy rescaling of O (only when the
+//              max grows by more than 2^8), P = exp2(S*scale*log2e - m) packed as
+//              bf16 into the TMEM columns of the S tile it came from.
 // The 512 value columns are split over two CTAs because O for 128 heads x 512
 // columns in f32 would fill all 512 TMEM columns; each CTA recomputes S.
 // With more than one split the CTAs write unnormalised partial O plus their
@@ -33,26 +35,23 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;  // warp 0 MMA, warps 1-3 gather, warps 4-7 softmax/epilogue
-constexpr int kGather = 96;
-constexpr int kRing = 8;
-constexpr int kTile = 64;
-constexpr int kChunks = 9;       // 576 / 64
-constexpr int kSOnly = 5;        // chunks used only by S (other half + rope)
+constexpr int kThreads = 256;  // warp 0 gather, warp 1 MMA, warps 2-3 idle, warps 4-7 softmax
+constexpr int kRing = 5;
+constexpr int kTile = 128;
+constexpr int kChunks = 9;  // 576 / 64
 constexpr int kHeads = 128;
 constexpr int kDqk = 576;
 constexpr int kHalf = 256;
 constexpr int kTargetCtas = 152;
+constexpr uint32_t kChunkBytes = kTile * 128;  // 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct MParams {
-  const uint16_t* kv;
-  int64_t kv_page_stride;  // bytes
-  int num_pages;
   const int32_t* bt;
   int64_t bt_stride;
+  int num_pages;
   int next_n;
   const int32_t* idx;
   int k;
@@ -66,24 +65,15 @@ struct MParams {
 };
 
 struct MSmem {
-  uint8_t q[kChunks][128 * 128];   // 9 x 16 KB, K-major SW128, rows = heads
-  uint8_t p[128 * 128];            // P tile [128 heads x 64 tokens] bf16, K-major SW128
-  uint8_t ring[kRing][kTile * 128];  // [64 tokens x 64 elems] bf16 SW128
-  const uint8_t* tokptr[2][kTile];
+  uint8_t q[kChunks][kHeads * 128];  // 9 x 16 KB, K-major SW128, rows = heads
+  uint8_t ring[kRing][kChunkBytes];  // [128 tokens x 64 elems] bf16 SW128
   uint64_t q_full;
-  uint64_t chunk_full[kRing], chunk_empty[kRing];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, pv_done;
+  uint64_t full[kRing], empty[kRing];
+  uint64_t s_full[2];
+  uint64_t p_full[2], pv_done[2];  // per S/P tile: tile t uses index t & 1
   uint32_t tmem_base;
   int abort;
 };
-
-__device__ __forceinline__ int chunk_of(int vh, int q) {
-  // S-only chunks first: the other half's four 64-wide blocks, then the rope block.
-  if (q < 4) return (vh ? 0 : 4) + q;
-  if (q == 4) return 8;
-  return 4 * vh + (q - 5);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
@@ -91,17 +81,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return lo | (hi << 16);
 }
 
-__device__ __forceinline__ float bf16_round(float a) {
-  return __bfloat162float(__float2bfloat16_rn(a));
-}
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const MParams p) {
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_kv, const MParams p) {
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescS = make_idesc(1, 1, 128, kTile, false, false);
-  constexpr uint32_t kIdescPV = make_idesc(1, 1, 128, 64, false, true);
-  constexpr int kSCol = 0;      // S buffers at columns [0, 128)
-  constexpr int kOCol = 128;    // O half at columns [128, 384)
+  constexpr int kSCol = 0;    // S/P tiles at columns [0, 256)
+  constexpr int kOCol = 256;  // O half at columns [256, 512)
   extern __shared__ uint8_t smem_raw[];
   MSmem& s = *reinterpret_cast<MSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
@@ -122,202 +111,226 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     mbar_init(&s.q_full, 1);
     for (int i = 0; i < kRing; ++i) {
-      mbar_init(&s.chunk_full[i], kGather);
-      mbar_init(&s.chunk_empty[i], 1);
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_empty[i], 4);
-    }
-    mbar_init(&s.p_full, 128);
-    mbar_init(&s.pv_done, 1);
+    mbar_init(&s.s_full[0], 1);
+    mbar_init(&s.s_full[1], 1);
+    // One arrival per softmax warp, one barrier per S/P tile: a warp can run one
+    // tile ahead of the others (S(i+1) does not wait for P(i)), never two (S(i+2)
+    // waits for PV(i)), so its arrival never lands in another tile's phase.
+    mbar_init(&s.p_full[0], 4);
+    mbar_init(&s.p_full[1], 4);
+    // PV(t) commits to pv_done[t & 1].  With one barrier per tile parity every
+    // waiter is within one phase of the phase it waits for (S(i) is issued only
+    // after PV(i-2) completed), so a parity wait cannot alias an older phase.
+    mbar_init(&s.pv_done[0], 1);
+    mbar_init(&s.pv_done[1], 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   volatile int* abort = &s.abort;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ MMA issuer --
-    if (ntile > 0 && mbar_wait(&s.q_full, 0, p.err, abort)) {
-      for (int i = 0; i < ntile && !*abort; ++i) {
-        const int buf = i & 1;
-        if (i >= 2 && !mbar_wait(&s.s_empty[buf], ((i >> 1) - 1) & 1, p.err, abort)) break;
-        tc_fence_after();
-        const uint32_t dS = s.tmem_base + kSCol + buf * kTile;
-        bool bad = false;
-        for (int qq = 0; qq < kChunks; ++qq) {
-          const int g = i * kChunks + qq;
-          const int slot = g % kRing;
-          if (!mbar_wait(&s.chunk_full[slot], (g / kRing) & 1, p.err, abort)) { bad = true; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t a0 = smem_u32(s.q[chunk_of(vh, qq)]);
-            const uint32_t b0 = smem_u32(s.ring[slot]);
+    // -------------------------------------------------------------- gather --
+    if (lane == 0 && ntile > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kv);
+      mbar_arrive_expect_tx(&s.q_full, kChunks * kHeads * 128);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_2d(s.q[c], &tm_q, &s.q_full, 64 * c, row * kHeads);
+    }
+    // Lane l fetches tokens 4l..4l+3 of a tile.  Latent rows (page*64 + slot)
+    // of tile i+1 are computed while tile i is issued: idx is read two tiles
+    // ahead, the block table one tile ahead.
+    auto load_toks = [&](int i, int (&t)[4]) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16(dS, sw128_desc(a0 + 32 * kk, 16, 1024), sw128_desc(b0 + 32 * kk, 16, 1024),
-                      kIdescS, (qq | kk) != 0);
-            if (qq < kSOnly) mma_commit(&s.chunk_empty[slot]);
+      for (int u = 0; u < 4; ++u) {
+        const int pos = s0 + i * kTile + 4 * lane + u;
+        t[u] = (i < ntile && pos < s1) ? idx_row[pos] : -1;
+      }
+    };
+    auto load_pages = [&](const int (&t)[4], int (&pg)[4]) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t pg_i = t[u] / 64;
+        pg[u] = (t[u] >= 0 && pg_i < p.bt_stride)
+                    ? p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i] : -1;
+      }
+    };
+    auto make_rows = [&](const int (&t)[4], const int (&pg)[4], int (&r)[4]) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        r[u] = -1;  // out of the tensor: TMA fills zeros
+        if (t[u] >= 0) {
+          if (pg[u] >= 0 && pg[u] < p.num_pages) r[u] = pg[u] * 64 + t[u] % 64;
+          else raise_error(p.err, kErrBadIndex);
+        }
+      }
+    };
+    int tk_next[4], rows_cur[4], rows_prev[4] = {-1, -1, -1, -1};
+    {
+      int t0[4], pg0[4];
+      load_toks(0, t0);
+      load_pages(t0, pg0);
+      make_rows(t0, pg0, rows_cur);
+      load_toks(1, tk_next);
+    }
+    int g = 0;  // ring sequence number
+    bool bad = false;
+    auto issue = [&](int c, const int (&r)[4]) -> bool {
+      const int slot = g % kRing;
+      if (g >= kRing && !mbar_wait_warp(&s.empty[slot], ((g / kRing) - 1) & 1, p.err, abort))
+        return false;
+      if (lane == 0) mbar_arrive_expect_tx(&s.full[slot], kChunkBytes);
+      __syncwarp();
+      tma_gather4(s.ring[slot] + lane * 512, &tm_kv, &s.full[slot], 64 * c, r[0], r[1], r[2], r[3]);
+      ++g;
+      return true;
+    };
+    for (int i = 0; i <= ntile && !bad; ++i) {
+      // loads for the next tiles go out first; their results are used after
+      // this tile's copies have been issued
+      int pg_next[4] = {-1, -1, -1, -1}, tk_after[4] = {-1, -1, -1, -1};
+      if (i + 1 < ntile) {
+        load_pages(tk_next, pg_next);
+        load_toks(i + 2, tk_after);
+      }
+      if (i < ntile)
+        for (int c = 0; c < kChunks && !bad; ++c) bad = !issue(c, rows_cur);
+      if (i >= 1)
+        for (int j = 0; j < 4 && !bad; ++j) bad = !issue(4 * vh + j, rows_prev);
+      int rows_next[4] = {-1, -1, -1, -1};
+      if (i + 1 < ntile) make_rows(tk_next, pg_next, rows_next);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        rows_prev[u] = rows_cur[u];
+        rows_cur[u] = rows_next[u];
+        tk_next[u] = tk_after[u];
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer --
+    if (ntile > 0 && mbar_wait_warp(&s.q_full, 0, p.err, abort)) {
+      int g = 0;
+      for (int i = 0; i <= ntile && !*abort; ++i) {
+        bool bad = false;
+        if (i < ntile) {
+          const int buf = i & 1;
+          // the S/P tile is reused after PV(i-2) has read P(i-2) from it
+          if (i >= 2 && !mbar_wait_warp(&s.pv_done[i & 1], ((i - 2) >> 1) & 1, p.err, abort)) break;
+          tc_fence_after();
+          const uint32_t dS = s.tmem_base + kSCol + buf * kTile;
+          for (int c = 0; c < kChunks; ++c, ++g) {
+            const int slot = g % kRing;
+            if (!mbar_wait_warp(&s.full[slot], (g / kRing) & 1, p.err, abort)) { bad = true; break; }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t a0 = smem_u32(s.q[c]);
+              const uint32_t b0 = smem_u32(s.ring[slot]);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16(dS, sw128_desc(a0 + 32 * kk, 16, 1024),
+                        sw128_desc(b0 + 32 * kk, 16, 1024), kIdescS, (c | kk) != 0);
+              mma_commit(&s.empty[slot]);
+            }
+            __syncwarp();
           }
+          if (bad) break;
+          if (lane == 0) mma_commit(&s.s_full[buf]);
           __syncwarp();
         }
-        if (bad) break;
-        if (lane == 0) mma_commit(&s.s_full[buf]);
-        __syncwarp();
-        if (!mbar_wait(&s.p_full, i & 1, p.err, abort)) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t pa = smem_u32(s.p);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int slot = (i * kChunks + kSOnly + j) % kRing;
-              const uint32_t vb = smem_u32(s.ring[slot]) + 2048 * kk;
-              mma_f16(s.tmem_base + kOCol + 64 * j, sw128_desc(pa + 32 * kk, 16, 1024),
-                      sw128_desc(vb, 8192, 1024), kIdescPV, (i > 0 || kk > 0));
-            }
+        if (i >= 1) {
+          const int t = i - 1;  // PV of the previous tile
+          if (!mbar_wait_warp(&s.p_full[t & 1], (t >> 1) & 1, p.err, abort)) break;
+          for (int j = 0; j < 4 && !bad; ++j) {
+            const int gg = g + j;
+            bad = !mbar_wait_warp(&s.full[gg % kRing], (gg / kRing) & 1, p.err, abort);
           }
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_commit(&s.chunk_empty[(i * kChunks + kSOnly + j) % kRing]);
-          mma_commit(&s.pv_done);
+          if (bad) break;
+          tc_fence_after();
+          if (lane == 0) {
+            // value chunk j sits in slot (g + j) % kRing: one or two contiguous runs
+            const int first = g % kRing;
+            const int n1 = min(4, kRing - first);  // chunks in the first run
+            const uint32_t pa = s.tmem_base + kSCol + (t & 1) * kTile;
+            const uint32_t v0 = smem_u32(s.ring[first]);
+            const uint32_t v1 = smem_u32(s.ring[0]);
+#pragma unroll 1
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+              mma_f16_ts(s.tmem_base + kOCol, pa + 8 * kk,
+                         sw128_desc(v0 + 2048 * kk, kChunkBytes, 1024),
+                         make_idesc(1, 1, 128, 64 * n1, false, true), acc);
+              if (n1 < 4)
+                mma_f16_ts(s.tmem_base + kOCol + 64 * n1, pa + 8 * kk,
+                           sw128_desc(v1 + 2048 * kk, kChunkBytes, 1024),
+                           make_idesc(1, 1, 128, 64 * (4 - n1), false, true), acc);
+            }
+            for (int j = 0; j < 4; ++j) mma_commit(&s.empty[(g + j) % kRing]);
+            mma_commit(&s.pv_done[t & 1]);
+          }
+          __syncwarp();
+          g += 4;
         }
-        __syncwarp();
       }
     }
-  } else if (warp < 4) {
-    // ---------------------------------------------------------------- gather --
-    const int gt = tid - 32;  // 0..95
-    if (gt == 0 && ntile > 0) {
-      tma_prefetch_desc(&tm_q);
-      mbar_arrive_expect_tx(&s.q_full, kChunks * 128 * 128);
-      for (int c = 0; c < kChunks; ++c) tma_load_2d(s.q[c], &tm_q, &s.q_full, 64 * c, row * kHeads);
-    }
-    const uint8_t* kvb = reinterpret_cast<const uint8_t*>(p.kv);
-    // Token pointers: idx is read two tiles ahead and the block table one tile
-    // ahead, so neither load sits on the path that issues a tile's copies.
-    auto load_tok = [&](int i) -> int {
-      const int pos = s0 + i * kTile + gt;
-      return (gt < kTile && i < ntile && pos < s1) ? idx_row[pos] : -1;
-    };
-    auto load_page = [&](int tok) -> int {
-      if (tok < 0) return -1;
-      const int64_t pg_i = tok / 64;
-      return pg_i < p.bt_stride ? p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i] : -1;
-    };
-    auto make_ptr = [&](int tok, int page) -> const uint8_t* {
-      if (tok < 0) return nullptr;
-      if (page < 0 || page >= p.num_pages) {
-        raise_error(p.err, kErrBadIndex);
-        return nullptr;
-      }
-      return kvb + static_cast<int64_t>(page) * p.kv_page_stride +
-             static_cast<int64_t>(tok % 64) * (kDqk * 2);
-    };
-    int tok_a = load_tok(0);
-    int tok_b = load_tok(1);
-    if (gt < kTile) s.tokptr[0][gt] = make_ptr(tok_a, load_page(tok_a));
-    constexpr int kDepth = 4;  // chunks kept in flight per thread
-    int issued = 0;            // chunks issued so far (global chunk counter)
-    int signalled = 0;
-    bool bad = false;
-    // Every gather thread passes exactly one named barrier per tile, even after
-    // an abort, so no thread can be left waiting on the barrier.
-    for (int i = 0; i < ntile; ++i) {
-      const int tb = i & 1;
-      named_bar_sync(1, kGather);
-      if (bad || *abort) {
-        bad = true;
-        continue;
-      }
-      int page_b = -1, tok_c = -1;
-      if (gt < kTile && i + 1 < ntile) {
-        page_b = load_page(tok_b);
-        tok_c = load_tok(i + 2);
-      }
-      for (int qq = 0; qq < kChunks; ++qq) {
-        const int g = i * kChunks + qq;
-        const int slot = g % kRing;
-        if (g >= kRing && !mbar_wait(&s.chunk_empty[slot], ((g / kRing) - 1) & 1, p.err, abort)) {
-          bad = true;
-          break;
-        }
-        const int c = chunk_of(vh, qq);
-        uint8_t* dst = s.ring[slot];
-        for (int piece = gt; piece < kTile * 8; piece += kGather) {
-          const int r = piece >> 3, ch = piece & 7;
-          const uint8_t* src = s.tokptr[tb][r];
-          uint8_t* d = dst + sw128_offset(r, ch);
-          if (src) cp_async_16(d, src + c * 128 + ch * 16);
-          else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-        }
-        cp_async_commit();
-        ++issued;
-        if (issued - signalled > kDepth) {
-          cp_async_wait<kDepth>();
-          fence_proxy_async_smem();
-          mbar_arrive(&s.chunk_full[signalled % kRing]);
-          ++signalled;
-        }
-      }
-      if (gt < kTile && i + 1 < ntile) {
-        s.tokptr[tb ^ 1][gt] = make_ptr(tok_b, page_b);
-        tok_b = tok_c;
-      }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (!bad)
-      while (signalled < issued) {
-        mbar_arrive(&s.chunk_full[signalled % kRing]);
-        ++signalled;
-      }
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------ softmax / epilogue --
     const int quad = warp & 3;
     const int h = quad * 32 + lane;  // head == TMEM lane
     const uint32_t lane_base = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     float m_run = -INFINITY, l_run = 0.f;
     bool bad = false;
-    // validity of a tile's 64 selections: lane j of every warp reads entries j
-    // and 32 + j, the two ballots give the tile's mask (read one tile ahead)
-    auto load_sel = [&](int i, int off) -> int {
-      const int pos = s0 + i * kTile + off + lane;
-      return (i < ntile && pos < s1) ? idx_row[pos] : -1;
+    // validity of a tile's 128 selections: lane j of every warp reads entries
+    // j, 32+j, 64+j, 96+j; four ballots give the tile's mask (read a tile ahead)
+    auto load_sel = [&](int i, int (&v)[4]) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pos = s0 + i * kTile + 32 * u + lane;
+        v[u] = (i < ntile && pos < s1) ? idx_row[pos] : -1;
+      }
     };
-    int sel_lo = load_sel(0, 0), sel_hi = load_sel(0, 32);
+    int sel[4];
+    load_sel(0, sel);
     for (int i = 0; i < ntile; ++i) {
-      const unsigned m_lo = __ballot_sync(0xffffffffu, sel_lo >= 0);
-      const unsigned m_hi = __ballot_sync(0xffffffffu, sel_hi >= 0);
-      sel_lo = load_sel(i + 1, 0);
-      sel_hi = load_sel(i + 1, 32);
+      unsigned m[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) m[u] = __ballot_sync(0xffffffffu, sel[u] >= 0);
+      load_sel(i + 1, sel);
       const int buf = i & 1;
-      if (!mbar_wait(&s.s_full[buf], (i >> 1) & 1, p.err, abort)) { bad = true; break; }
+      if (!mbar_wait_warp(&s.s_full[buf], (i >> 1) & 1, p.err, abort)) { bad = true; break; }
       tc_fence_after();
+      const uint32_t sbase = lane_base + kSCol + buf * kTile;
       float x[kTile];
-      tmem_ld64_sync(lane_base + kSCol + buf * kTile, x);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.s_empty[buf]);
+      {
+        float a[64], b[64];
+        tmem_ld64_sync(sbase, a);
+        tmem_ld64_sync(sbase + 64, b);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          x[j] = a[j];
+          x[64 + j] = b[j];
+        }
+      }
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kTile; ++j) {
-        const bool ok = ((j < 32 ? (m_lo >> j) : (m_hi >> (j - 32))) & 1u) != 0;
+        const bool ok = ((m[j >> 5] >> (j & 31)) & 1u) != 0;
         x[j] = ok ? x[j] * p.scale_log2 : -INFINITY;
         mt = fmaxf(mt, x[j]);
       }
-      // PV(i-1) must be complete before P is overwritten or O rescaled
-      if (i > 0 && !mbar_wait(&s.pv_done, (i - 1) & 1, p.err, abort)) { bad = true; break; }
-      tc_fence_after();
       const bool grow = mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY);
       const float m_new = grow ? mt : m_run;
       const bool need_rescale = grow && i > 0 && m_run > -INFINITY;
       const float corr = need_rescale ? exp2f(m_run - m_new) : 1.f;
       if (__any_sync(0xffffffffu, need_rescale)) {
+        // O must hold PV(i-1) complete before it is rescaled
+        if (!mbar_wait_warp(&s.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err, abort)) { bad = true; break; }
+        tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < kHalf / 32; ++cc) {
           float o[32];
@@ -330,29 +343,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_run *= corr;
       m_run = m_new;
-      // P = exp2(x - m) in bf16, row h of the swizzled P tile
-      uint8_t* prow = s.p + h * 128;
+      // P = exp2(x - m) as packed bf16 over the first 64 columns of this S tile
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float e[8];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          e[j] = m_run == -INFINITY ? 0.f : exp2f(x[8 * ch + j] - m_run);
-          l_run += bf16_round(e[j]);
+        for (int j = 0; j < 32; ++j) {
+          const float e0 = m_run == -INFINITY ? 0.f : exp2f(x[64 * half + 2 * j] - m_run);
+          const float e1 = m_run == -INFINITY ? 0.f : exp2f(x[64 * half + 2 * j + 1] - m_run);
+          pk[j] = pack_bf16(e0, e1);
+          l_run += bf16_lo(pk[j]) + bf16_hi(pk[j]);
         }
-        uint4 v;
-        v.x = pack_bf16(e[0], e[1]);
-        v.y = pack_bf16(e[2], e[3]);
-        v.z = pack_bf16(e[4], e[5]);
-        v.w = pack_bf16(e[6], e[7]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (h & 7)) << 4)) = v;
+        tmem_st32_sync(sbase + 32 * half, pk);
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&s.p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.p_full[buf]);
     }
     // ---- epilogue: O half of this CTA ----
-    if (!bad && ntile > 0 && mbar_wait(&s.pv_done, (ntile - 1) & 1, p.err, abort)) {
+    if (!bad && ntile > 0 &&
+        mbar_wait_warp(&s.pv_done[(ntile - 1) & 1], ((ntile - 1) >> 1) & 1, p.err, abort)) {
       tc_fence_after();
       if (p.nsplit == 1) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -408,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(s.tmem_base, kTmemCols);
   }
@@ -465,27 +475,34 @@ size_t mla_workspace_size(int R, int k) {
 }
 
 cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  (void)dev;
   const int R = a.num_req * a.next_n;
   const int ns = choose_nsplit(R, a.k);
   const int tiles = (a.k + kTile - 1) / kTile;
   const int tps = ((tiles + ns - 1) / ns) * kTile;
-  CUtensorMap tq;
+  CUtensorMap tq, tkv;
+  char msg[128];
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(R) * kHeads};
     const uint64_t strides[1] = {kDqk * 2};
     const uint32_t box[2] = {64, 128};
-    char msg[128];
     if (!encode_tensor_map(&tq, 1, 2, const_cast<uint16_t*>(a.q), dims, strides, box, true, msg,
                            sizeof(msg)))
       return cudaErrorInvalidValue;
   }
+  {
+    // latent cache as [num_pages * 64 rows, 576] bf16 (pages are contiguous)
+    const uint64_t dims[2] = {static_cast<uint64_t>(kDqk),
+                              static_cast<uint64_t>(a.num_pages) * 64};
+    const uint64_t strides[1] = {kDqk * 2};
+    const uint32_t box[2] = {64, 1};
+    if (!encode_tensor_map(&tkv, 1, 2, const_cast<uint16_t*>(a.kv), dims, strides, box, true, msg,
+                           sizeof(msg)))
+      return cudaErrorInvalidValue;
+  }
   MParams p;
-  p.kv = a.kv;
-  p.kv_page_stride = a.kv_page_stride;
-  p.num_pages = a.num_pages;
   p.bt = a.block_table;
   p.bt_stride = a.bt_stride;
+  p.num_pages = a.num_pages;
   p.next_n = a.next_n;
   p.idx = a.idx;
   p.k = a.k;
@@ -501,13 +518,12 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  sparse_mla_kernel<<<dim3(R, 2, ns), kThreads, smem, stream>>>(tq, p);
+  sparse_mla_kernel<<<dim3(R, 2, ns), kThreads, smem, stream>>>(tq, tkv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
   mla_combine_kernel<<<dim3(R, 2), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
-
 
 // ------------------------------------------------ no-allocation variant --
 // Split-K scratch for callers that cannot allocate device memory.  The array

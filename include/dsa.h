@@ -162,7 +162,8 @@ dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int
  *
  *   q         device [R, 128, 576] bf16.
  *   kv_cache  device; page p = [64, 576] bf16 at kv_cache + p * kv_page_stride
- *             bytes (16-byte aligned, stride % 16 == 0).
+ *             bytes; the pages must be contiguous (kv_page_stride == 73728) and
+ *             kv_cache 16-byte aligned (the gathers use one TMA map over the cache).
  *   idx       device [R, k] int32, 1 <= k <= DSA_MAX_TOPK.
  *   out       device [R, 128, 512] bf16.   lse  device [R, 128] f32 (may be NULL).
  *   workspace device, dsa_sparse_mla_workspace_size(R, k) bytes (split-K
