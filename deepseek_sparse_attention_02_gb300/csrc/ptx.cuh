@@ -114,19 +114,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Four rows (r0..r3) of a 2-D tensor map, columns [x, x + box width), into
-// consecutive box-sized rows at dst (the map's swizzle applies).  Rows outside
-// the tensor read as zeros.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int x, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2),
-      "r"(r3)
-      : "memory");
-}
-
 // Plain (untiled) bulk copy global -> shared; 16-byte aligned, size % 16 == 0.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -135,13 +122,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Asynchronously pulls [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
-               "r"(bytes)
-               : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later
@@ -156,8 +136,19 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
                "l"(reinterpret_cast<uint64_t>(src))
                : "memory");
 }
+// Zero-fills the 16 destination bytes without reading the source (src-size 0).
+__device__ __forceinline__ void cp_async_16_zero(void* dst, const void* any_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(any_src))
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Arrive on the mbarrier once all cp.async issued so far by this thread have
+// completed (the arrival is counted against the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

@@ -5,21 +5,25 @@
 //
 // Work unit = one CTA per (row, value half vh, split); 128 selected tokens per
 // tile.
-//   warp 0     gather producer: Q of the row once (TMA, nine 128B-swizzled
-//              [128 x 64] K-chunks); then per tile the nine [128 tokens x 64]
-//              K-chunks of the selected latents, and one tile later the four
-//              value chunks of this CTA's half again (an L2 hit), through a
-//              5-slot ring of 16 KB, by TMA tile::gather4 (each lane fetches 4
-//              rows; a skipped selection reads an out-of-range row = zeros);
-//   warp 1     tcgen05 issuer, in the order S(0), S(1), PV(0), S(2), PV(1), ...:
+//   warps 0-7  gather: Q of the row once (TMA, nine 128B-swizzled [128 x 64]
+//              K-chunks); then per tile the nine [128 tokens x 64] K-chunks of
+//              the selected latents, and one tile later the four value chunks
+//              of this CTA's half again (an L2 hit), through a 5-slot ring of
+//              16 KB, by 16-byte cp.async (each thread copies 4 pieces of a
+//              chunk; completion is signalled with cp.async.mbarrier.arrive, so
+//              no thread waits for its copies; a skipped selection is
+//              zero-filled);
+//   warps 8-11 softmax (one thread per head / TMEM lane): mask skipped
+//              selections, running max with lazy rescaling of O (only when the
+//              max grows by more than 2^8), P = exp2(S*scale*log2e - m) packed as
+//              bf16 into the TMEM columns of the S tile it came from;
+//   warp 12    tcgen05 issuer, in the order S(0), S(1), PV(0), S(2), PV(1), ...:
 //              S = Q K^T (kind::f16, M = 128 heads, N = 128 tokens, K = 576)
 //              into one of two TMEM tiles; O[128 x 256] += P V_half with P read
 //              from TMEM and V read MN-major from the ring (N = 256 when the
-//              four value chunks are contiguous in the ring, else two MMAs);
-//   warps 4-7  softmax (one thread per head / TMEM lane): mask skipped
-//              selections, running max with lazy rescaling of O (only when the
-//              max grows by more than 2^8), P = exp2(S*scale*log2e - m) packed as
-//              bf16 into the TMEM columns of the S tile it came from.
+//              four value chunks are contiguous in the ring, else two MMAs).
+// Many gathering warps matter: scattered 128-byte latent lines reach ~4-5 TB/s
+// this way, about twice the rate of TMA tile::gather4 for the same lines.
 // The 512 value columns are split over two CTAs because O for 128 heads x 512
 // columns in f32 would fill all 512 TMEM columns; each CTA recomputes S.
 // With more than one split the CTAs write unnormalised partial O plus their
@@ -35,7 +39,9 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;  // warp 0 gather, warp 1 MMA, warps 2-3 idle, warps 4-7 softmax
+constexpr int kGatherWarps = 8;
+constexpr int kThreads = 32 * (kGatherWarps + 4 + 1);  // gather, softmax, MMA
+constexpr int kMmaWarp = kGatherWarps + 4;
 constexpr int kRing = 5;
 constexpr int kTile = 128;
 constexpr int kChunks = 9;  // 576 / 64
@@ -49,6 +55,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct MParams {
+  const uint8_t* kv;  // latent cache base: row r (page*64 + slot) at kv + r * 1152
   const int32_t* bt;
   int64_t bt_stride;
   int num_pages;
@@ -85,8 +92,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_kv, const MParams p) {
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const MParams p) {
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescS = make_idesc(1, 1, 128, kTile, false, false);
   constexpr int kSCol = 0;    // S/P tiles at columns [0, 256)
@@ -111,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     mbar_init(&s.q_full, 1);
     for (int i = 0; i < kRing; ++i) {
-      mbar_init(&s.full[i], 1);
+      mbar_init(&s.full[i], 32 * kGatherWarps);  // one cp.async completion per gather thread
       mbar_init(&s.empty[i], 1);
     }
     mbar_init(&s.s_full[0], 1);
@@ -128,28 +134,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.pv_done[1], 1);
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   volatile int* abort = &s.abort;
 
-  if (warp == 0) {
+  if (warp < kGatherWarps) {
     // -------------------------------------------------------------- gather --
-    if (lane == 0 && ntile > 0) {
+    const int gt = tid;  // 0 .. 32*kGatherWarps-1
+    if (gt == 0 && ntile > 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kv);
       mbar_arrive_expect_tx(&s.q_full, kChunks * kHeads * 128);
       for (int c = 0; c < kChunks; ++c)
         tma_load_2d(s.q[c], &tm_q, &s.q_full, 64 * c, row * kHeads);
     }
-    // Lane l fetches tokens 4l..4l+3 of a tile.  Latent rows (page*64 + slot)
-    // of tile i+1 are computed while tile i is issued: idx is read two tiles
-    // ahead, the block table one tile ahead.
+    // Thread gt copies, of every 16 KB chunk, the 16-byte pieces gt + 256 q
+    // (q = 0..3): chunk row (gt >> 3) + 32 q, piece gt & 7.  Its 4 latent rows
+    // (page*64 + slot, -1 = skipped) of tile i+1 are computed while tile i is
+    // issued: idx is read two tiles ahead, the block table one tile ahead.
+    constexpr int kRowStep = (32 * kGatherWarps) / 8;  // 32 rows between a thread's pieces
+    const int prow = gt >> 3, pch = gt & 7;
     auto load_toks = [&](int i, int (&t)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int pos = s0 + i * kTile + 4 * lane + u;
+        const int pos = s0 + i * kTile + prow + kRowStep * u;
         t[u] = (i < ntile && pos < s1) ? idx_row[pos] : -1;
       }
     };
@@ -164,10 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto make_rows = [&](const int (&t)[4], const int (&pg)[4], int (&r)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        r[u] = -1;  // out of the tensor: TMA fills zeros
+        r[u] = -1;
         if (t[u] >= 0) {
           if (pg[u] >= 0 && pg[u] < p.num_pages) r[u] = pg[u] * 64 + t[u] % 64;
-          else raise_error(p.err, kErrBadIndex);
+          else if (pch == 0) raise_error(p.err, kErrBadIndex);
         }
       }
     };
@@ -185,9 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = g % kRing;
       if (g >= kRing && !mbar_wait_warp(&s.empty[slot], ((g / kRing) - 1) & 1, p.err, abort))
         return false;
-      if (lane == 0) mbar_arrive_expect_tx(&s.full[slot], kChunkBytes);
-      __syncwarp();
-      tma_gather4(s.ring[slot] + lane * 512, &tm_kv, &s.full[slot], 64 * c, r[0], r[1], r[2], r[3]);
+      uint8_t* dst = s.ring[slot];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint8_t* d = dst + sw128_offset(prow + kRowStep * u, pch);
+        if (r[u] >= 0)
+          cp_async_16(d, p.kv + static_cast<int64_t>(r[u]) * (kDqk * 2) + c * 128 + pch * 16);
+        else
+          cp_async_16_zero(d, p.kv);
+      }
+      cp_async_mbar_arrive_noinc(&s.full[slot]);
       ++g;
       return true;
     };
@@ -212,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tk_next[u] = tk_after[u];
       }
     }
-  } else if (warp == 1) {
+    cp_async_wait<0>();  // no copy of this thread is left in flight at exit
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
     if (ntile > 0 && mbar_wait_warp(&s.q_full, 0, p.err, abort)) {
       int g = 0;
@@ -227,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kChunks; ++c, ++g) {
             const int slot = g % kRing;
             if (!mbar_wait_warp(&s.full[slot], (g / kRing) & 1, p.err, abort)) { bad = true; break; }
+            fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core
             tc_fence_after();
             if (lane == 0) {
               const uint32_t a0 = smem_u32(s.q[c]);
@@ -251,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bad = !mbar_wait_warp(&s.full[gg % kRing], (gg / kRing) & 1, p.err, abort);
           }
           if (bad) break;
+          fence_proxy_async_smem();
           tc_fence_after();
           if (lane == 0) {
             // value chunk j sits in slot (g + j) % kRing: one or two contiguous runs
@@ -278,9 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------ softmax / epilogue --
-    const int quad = warp & 3;
+    const int quad = warp & 3;  // warps 8-11: TMEM lane quadrants 0-3
     const int h = quad * 32 + lane;  // head == TMEM lane
     const uint32_t lane_base = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     float m_run = -INFINITY, l_run = 0.f;
@@ -305,23 +324,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(&s.s_full[buf], (i >> 1) & 1, p.err, abort)) { bad = true; break; }
       tc_fence_after();
       const uint32_t sbase = lane_base + kSCol + buf * kTile;
-      float x[kTile];
-      {
-        float a[64], b[64];
-        tmem_ld64_sync(sbase, a);
-        tmem_ld64_sync(sbase + 64, b);
+      // scores of tokens j (column j of the tile) in log2 units, -inf if skipped
+      auto scaled = [&](float (&v)[64], int half) {
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          x[j] = a[j];
-          x[64 + j] = b[j];
+          const int t = 64 * half + j;
+          const bool ok = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
+          v[j] = ok ? v[j] * p.scale_log2 : -INFINITY;
         }
-      }
+      };
       float mt = -INFINITY;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float v[64];
+        tmem_ld64_sync(sbase + 64 * half, v);
+        scaled(v, half);
 #pragma unroll
-      for (int j = 0; j < kTile; ++j) {
-        const bool ok = ((m[j >> 5] >> (j & 31)) & 1u) != 0;
-        x[j] = ok ? x[j] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[j]);
+        for (int j = 0; j < 64; ++j) mt = fmaxf(mt, v[j]);
       }
       const bool grow = mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY);
       const float m_new = grow ? mt : m_run;
@@ -343,14 +362,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_run *= corr;
       m_run = m_new;
-      // P = exp2(x - m) as packed bf16 over the first 64 columns of this S tile
-#pragma unroll
+      // P = exp2(x - m) as packed bf16 over the first 64 columns of this S tile:
+      // tokens 0..63 -> columns 0..31 first (their scores are re-read before
+      // anything is written), then tokens 64..127 -> columns 32..63.
+#pragma unroll 1
       for (int half = 0; half < 2; ++half) {
+        float v[64];
+        tmem_ld64_sync(sbase + 64 * half, v);
+        scaled(v, half);
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float e0 = m_run == -INFINITY ? 0.f : exp2f(x[64 * half + 2 * j] - m_run);
-          const float e1 = m_run == -INFINITY ? 0.f : exp2f(x[64 * half + 2 * j + 1] - m_run);
+          const float e0 = m_run == -INFINITY ? 0.f : exp2f(v[2 * j] - m_run);
+          const float e1 = m_run == -INFINITY ? 0.f : exp2f(v[2 * j + 1] - m_run);
           pk[j] = pack_bf16(e0, e1);
           l_run += bf16_lo(pk[j]) + bf16_hi(pk[j]);
         }
@@ -418,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(s.tmem_base, kTmemCols);
   }
@@ -479,7 +503,7 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   const int ns = choose_nsplit(R, a.k);
   const int tiles = (a.k + kTile - 1) / kTile;
   const int tps = ((tiles + ns - 1) / ns) * kTile;
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   char msg[128];
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(R) * kHeads};
@@ -489,17 +513,8 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
                            sizeof(msg)))
       return cudaErrorInvalidValue;
   }
-  {
-    // latent cache as [num_pages * 64 rows, 576] bf16 (pages are contiguous)
-    const uint64_t dims[2] = {static_cast<uint64_t>(kDqk),
-                              static_cast<uint64_t>(a.num_pages) * 64};
-    const uint64_t strides[1] = {kDqk * 2};
-    const uint32_t box[2] = {64, 1};
-    if (!encode_tensor_map(&tkv, 1, 2, const_cast<uint16_t*>(a.kv), dims, strides, box, true, msg,
-                           sizeof(msg)))
-      return cudaErrorInvalidValue;
-  }
   MParams p;
+  p.kv = reinterpret_cast<const uint8_t*>(a.kv);
   p.bt = a.block_table;
   p.bt_stride = a.bt_stride;
   p.num_pages = a.num_pages;
@@ -518,7 +533,7 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  sparse_mla_kernel<<<dim3(R, 2, ns), kThreads, smem, stream>>>(tq, tkv, p);
+  sparse_mla_kernel<<<dim3(R, 2, ns), kThreads, smem, stream>>>(tq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
   mla_combine_kernel<<<dim3(R, 2), 256, 0, stream>>>(p);
