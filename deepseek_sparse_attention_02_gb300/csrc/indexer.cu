@@ -7,14 +7,21 @@
 // (a chunk = up to kChunkTiles tiles of 128 tokens of one row group; a row
 // group = up to 4 query rows of one request, which read the same keys).
 //
-//   warp 0      TMA producer: two 64-token key pages per tile
+//   warps 0-3   TMA producers, warp w issuing the tiles t == w (mod 4) of
+//               the CTA: two 64-token key pages per tile
 //               (cp.async.bulk.tensor, 128-byte swizzle) + their 2 x 256 B
-//               of per-token scales (cp.async.bulk); the group's q (one 2-D
-//               TMA box of N = 64*rows rows) and w*sq into a Q slot.
-//   warp 1      tcgen05 issuer: D[128 tokens, N] = K[128, 128] * Q[N, 128]^T,
-//               four kind::f8f6f4 MMAs (K = 32 each) into one of two TMEM
-//               accumulators.
-//   warps 2-9   two epilogue warpgroups, one per TMEM accumulator: each
+//               of per-token scales (cp.async.bulk).  Warp 0 also puts the
+//               group's q (one 2-D TMA box of N = 64*rows rows) and w*sq
+//               into a Q slot.  One issuing warp alone does not keep enough
+//               page copies in flight to reach the HBM rate on GB300.
+//   warp 4      tcgen05 issuer: D[128 tokens, N] = K[128, 128] * Q[N, 128]^T,
+//               four kind::f8f6f4 MMAs (K = 32 each) into one of kAcc(G) TMEM
+//               accumulators (4 when 4*N columns fit in TMEM, else 2): the
+//               MMA of tile i waits for the epilogue of tile i - kAcc, so
+//               more accumulators take the MMA -> epilogue latency off the
+//               load path.
+//   warps 5-12  two epilogue warpgroups, warpgroup w draining the tiles
+//               t == w (mod 2) (hence the accumulators a == w (mod 2)): each
 //               thread owns one token (one TMEM lane) and reduces
 //               sum_h w'_h * max(d_h, 0) per row, times s_t, and stores the
 //               row's logit (consecutive threads -> consecutive tokens).
@@ -30,8 +37,12 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kProducerWarps = 4;  // divides kStages: a stage is always filled by one warp
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kFirstEpiWarp = kMmaWarp + 1;
+constexpr int kThreads = 32 * (kFirstEpiWarp + 8);
 constexpr int kStages = 8;
+static_assert(kStages % kProducerWarps == 0, "stage -> producer warp must be fixed");
 constexpr int kTileTokens = 128;
 constexpr uint32_t kPageKeyBytes = 64 * 128;  // 8192
 constexpr uint32_t kStageBytes = 2 * kPageKeyBytes;
@@ -155,7 +166,7 @@ struct Smem {
   int prefix[kMaxReq + 1];
   uint64_t full[kStages], empty[kStages];
   uint64_t qfull[2], qempty[2];
-  uint64_t tfull[2], tempty[2];
+  uint64_t tfull[4], tempty[4];
   uint32_t tmem_base;
   int abort;
   int scan_tmp[kThreads];
@@ -166,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const KParams p) {
   constexpr int N = 64 * G;
-  constexpr uint32_t kTmemCols = (2 * N <= 128) ? 128 : (2 * N <= 256 ? 256 : 512);
+  constexpr int kAcc = 4 * N <= 512 ? 4 : 2;
+  constexpr uint32_t kTmemCols = (kAcc * N <= 128) ? 128 : (kAcc * N <= 256 ? 256 : 512);
   constexpr uint32_t kIdesc = make_idesc(0, 0, 128, N, false, false);
   using S = Smem<G>;
   extern __shared__ uint8_t smem_raw[];
@@ -233,15 +245,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1 + 4);  // MMA commit + the 4 epilogue warps that read the scales
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.qfull[i], 32);     // the 32 producer lanes (w*sq) + TMA bytes
-      mbar_init(&s.qempty[i], 1 + 8); // MMA commit + 8 epilogue warps
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);
+      mbar_init(&s.tempty[i], 4);  // the 4 warps of the warpgroup that drains accumulator i
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.qfull[i], 32);     // the 32 lanes of producer warp 0 (w*sq) + TMA bytes
+      mbar_init(&s.qempty[i], 1 + 8); // MMA commit + 8 epilogue warps
     }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -251,13 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c1 = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
   volatile int* abort = &s.abort;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer --
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ producers --
     Cursor cur;
     cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_q);
+      if (warp == 0) tma_prefetch_desc(&tm_q);
     }
     // Page ids of a chunk (at most 2 * kChunkTiles) are loaded by the lanes of
     // this warp one chunk ahead, so no block-table load sits on the TMA issue path.
@@ -277,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (cur.valid() && !*abort) {
       const int r0 = cur.row0();
       const int nr = cur.nrows();
-      if (new_group) {
+      if (new_group && warp == 0) {
         const int slot = cur.gcount & 1;
         const int use = cur.gcount >> 1;
         if (use > 0 && !mbar_wait_warp(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
@@ -299,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tb = cur.tile_begin();
       bool bad = false;
       for (int t = tb; t < cur.tile_end(); ++t, ++lt) {
+        if (lt % kProducerWarps != warp) continue;
         const int st = lt % kStages;
         const int use = lt / kStages;
         if (use > 0 && !mbar_wait_warp(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
@@ -331,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pages_next = chunk_pages(ahead);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------- MMA issuer --
     Cursor cur;
     cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
@@ -344,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool bad = false;
       for (int t = tb; t < te; ++t, ++lt) {
         const int st = lt % kStages;
-        const int buf = lt & 1;
-        const int ub = lt >> 1;
+        const int buf = lt % kAcc;
+        const int ub = lt / kAcc;
         if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
         if (ub > 0 && !mbar_wait_warp(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue --
-    const int wg = (warp - 2) >> 2;  // which accumulator this warpgroup drains
+    const int wg = (warp - kFirstEpiWarp) >> 2;  // which accumulator this warpgroup drains
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
     const int row_in_tile = quad * 32 + lane;
     Cursor cur;
@@ -388,12 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           waited_q = true;
         }
         const int st = lt % kStages;
-        if (!mbar_wait_warp(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
+        const int buf = lt % kAcc;
+        if (!mbar_wait_warp(&s.tfull[buf], (lt / kAcc) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
+        // the MMA has read the stage's keys (tfull); once every lane holds its
+        // scale the stage can be refilled
         const float sc = s.scales[st][row_in_tile];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[st]);
         const int tok = t * kTileTokens + row_in_tile;
         const uint32_t taddr = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(wg * N);
+                               static_cast<uint32_t>(buf * N);
 #pragma unroll
         for (int j = 0; j < G; ++j) {
           float v[64];
@@ -407,10 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&s.tempty[wg]);
-          mbar_arrive(&s.empty[st]);
-        }
+        if (lane == 0) mbar_arrive(&s.tempty[buf]);
       }
       if (bad) break;
       // A warp may walk through a group without processing any of its tiles (they
@@ -427,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(s.tmem_base, kTmemCols);
   }
