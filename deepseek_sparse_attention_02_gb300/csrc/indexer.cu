@@ -7,20 +7,24 @@
 // (a chunk = up to kChunkTiles tiles of 128 tokens of one row group; a row
 // group = up to 4 query rows of one request, which read the same keys).
 //
-//   warps 0-3   TMA producers, warp w issuing the tiles t == w (mod 4) of
-//               the CTA: two 64-token key pages per tile
+//   warps 0-3   TMA producers, warp w filling the key stages s == w (mod 4)
+//               (tile i of the CTA goes to stage i mod kStages): two 64-token
+//               key pages per tile
 //               (cp.async.bulk.tensor, 128-byte swizzle) + their 2 x 256 B
 //               of per-token scales (cp.async.bulk).  Warp 0 also puts the
 //               group's q (one 2-D TMA box of N = 64*rows rows) and w*sq
 //               into a Q slot.  One issuing warp alone does not keep enough
 //               page copies in flight to reach the HBM rate on GB300.
-//   warp 4      tcgen05 issuer: D[128 tokens, N] = K[128, 128] * Q[N, 128]^T,
-//               four kind::f8f6f4 MMAs (K = 32 each) into one of kAcc(G) TMEM
-//               accumulators (4 when 4*N columns fit in TMEM, else 2): the
-//               MMA of tile i waits for the epilogue of tile i - kAcc, so
-//               more accumulators take the MMA -> epilogue latency off the
-//               load path.
-//   warps 5-12  two epilogue warpgroups, warpgroup w draining the tiles
+//   warps 4-5   tcgen05 issuers (one thread each, warp 4 + m taking the
+//               tiles i == m (mod 2)): D[128 tokens, N] = K[128, 128] *
+//               Q[N, 128]^T, four kind::f8f6f4 MMAs (K = 32 each) into one of
+//               kAcc(G) TMEM accumulators (4 when 4*N columns fit in TMEM,
+//               else 2).  The MMA of tile i waits for the epilogue of tile
+//               i - kAcc, so more accumulators take the MMA -> epilogue
+//               latency off the load path; an M=128 MMA holds the issuing
+//               thread for ~96 cycles, so two issuers let one wait on its
+//               barriers while the other feeds the tensor pipe.
+//   warps 6-13  two epilogue warpgroups, warpgroup w draining the tiles
 //               t == w (mod 2) (hence the accumulators a == w (mod 2)): each
 //               thread owns one token (one TMEM lane) and reduces
 //               sum_h w'_h * max(d_h, 0) per row, times s_t, and stores the
@@ -37,12 +41,15 @@
 namespace dsa {
 namespace {
 
-constexpr int kProducerWarps = 4;  // divides kStages: a stage is always filled by one warp
-constexpr int kMmaWarp = kProducerWarps;
-constexpr int kFirstEpiWarp = kMmaWarp + 1;
+constexpr int kProducerWarps = 4;  // stage st is always filled by producer warp st % 4
+constexpr int kMmaWarp = kProducerWarps;  // first MMA warp (also owns the TMEM allocation)
+constexpr int kMmaWarps = 2;               // divides kAcc: an accumulator has one issuer
+constexpr int kFirstEpiWarp = kMmaWarp + kMmaWarps;
 constexpr int kThreads = 32 * (kFirstEpiWarp + 8);
-constexpr int kStages = 8;
-static_assert(kStages % kProducerWarps == 0, "stage -> producer warp must be fixed");
+// Key stages (a stage is held from its copy's issue until the epilogue has seen
+// its MMAs complete).  Ten stages for up to two rows per group measured no
+// faster than eight on GB300.
+__host__ __device__ constexpr int stages_for(int) { return 8; }
 constexpr int kTileTokens = 128;
 constexpr uint32_t kPageKeyBytes = 64 * 128;  // 8192
 constexpr uint32_t kStageBytes = 2 * kPageKeyBytes;
@@ -159,6 +166,7 @@ template <int G>
 struct Smem {
   static constexpr int N = 64 * G;
   static constexpr uint32_t kQBytes = N * 128;
+  static constexpr int kStages = stages_for(G);
   uint8_t keys[kStages][kStageBytes];  // 1024-aligned stage tiles
   uint8_t q[2][kQBytes];
   float scales[kStages][kTileTokens];
@@ -178,9 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const KParams p) {
   constexpr int N = 64 * G;
   constexpr int kAcc = 4 * N <= 512 ? 4 : 2;
+  static_assert(kAcc % kMmaWarps == 0, "an accumulator must have a single MMA issuer");
   constexpr uint32_t kTmemCols = (kAcc * N <= 128) ? 128 : (kAcc * N <= 256 ? 256 : 512);
   constexpr uint32_t kIdesc = make_idesc(0, 0, 128, N, false, false);
   using S = Smem<G>;
+  constexpr int kStages = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -243,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1 + 4);  // MMA commit + the 4 epilogue warps that read the scales
+      mbar_init(&s.empty[i], 4);  // the 4 epilogue warps of the tile (after tfull, so the MMA is done)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.qfull[i], 32);     // the 32 lanes of producer warp 0 (w*sq) + TMA bytes
-      mbar_init(&s.qempty[i], 1 + 8); // MMA commit + 8 epilogue warps
+      mbar_init(&s.qempty[i], kMmaWarps + 8); // MMA commits + 8 epilogue warps
     }
     fence_mbar_init();
   }
@@ -313,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tb = cur.tile_begin();
       bool bad = false;
       for (int t = tb; t < cur.tile_end(); ++t, ++lt) {
-        if (lt % kProducerWarps != warp) continue;
+        if ((lt % kStages) % kProducerWarps != warp) continue;
         const int st = lt % kStages;
         const int use = lt / kStages;
         if (use > 0 && !mbar_wait_warp(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
@@ -346,45 +356,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         pages_next = chunk_pages(ahead);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA issuer --
-    Cursor cur;
-    cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
-    int lt = 0;
-    bool new_group = true;
-    while (cur.valid() && !*abort) {
-      const int slot = cur.gcount & 1;
-      if (new_group && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
-      const int tb = cur.tile_begin(), te = cur.tile_end();
-      bool bad = false;
-      for (int t = tb; t < te; ++t, ++lt) {
-        const int st = lt % kStages;
-        const int buf = lt % kAcc;
-        const int ub = lt / kAcc;
-        if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
-        if (ub > 0 && !mbar_wait_warp(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
-        tc_fence_after();
-        if (lane == 0) {
+  } else if (warp < kFirstEpiWarp) {
+    // ---------------------------------------------------------- MMA issuers --
+    // One thread per MMA warp: the per-tile loop is on the critical path of the
+    // pipeline, so it carries no warp votes or warp barriers.
+    const int m = warp - kMmaWarp;
+    if (lane == 0) {
+      Cursor cur;
+      cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
+      int lt = 0;
+      bool new_group = true;
+      while (cur.valid() && !*abort) {
+        const int slot = cur.gcount & 1;
+        if (new_group && !mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+        const int tb = cur.tile_begin(), te = cur.tile_end();
+        bool bad = false;
+        const uint32_t b0 = smem_u32(s.q[slot]);
+        for (int t = tb; t < te; ++t, ++lt) {
+          if (lt % kMmaWarps != m) continue;
+          const int st = lt % kStages;
+          const int buf = lt % kAcc;
+          const int ub = lt / kAcc;
+          if (!mbar_wait(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
+          if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
+          tc_fence_after();
           const uint32_t a0 = smem_u32(s.keys[st]);
-          const uint32_t b0 = smem_u32(s.q[slot]);
           const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * N);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_f8f6f4(d, sw128_desc(a0 + 32 * k, 16, 1024), sw128_desc(b0 + 32 * k, 16, 1024),
                        kIdesc, k > 0);
-          mma_commit(&s.empty[st]);
+          // completion of these MMAs also frees the key stage: the epilogue
+          // releases it after it has seen tfull
           mma_commit(&s.tfull[buf]);
         }
-        __syncwarp();
+        if (bad) break;
+        new_group = cur.next();
+        if (new_group) mma_commit(&s.qempty[slot]);
       }
-      if (bad) break;
-      new_group = cur.next();
-      if (new_group && lane == 0) mma_commit(&s.qempty[slot]);
-      __syncwarp();
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------- epilogue --
-    const int wg = (warp - kFirstEpiWarp) >> 2;  // which accumulator this warpgroup drains
+    const int wg = (warp - kFirstEpiWarp) >> 2;  // which tiles (and accumulators) it drains
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
     const int row_in_tile = quad * 32 + lane;
     Cursor cur;
@@ -453,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int G>
 cudaError_t launch_g(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t stream,
                      const CUtensorMap& tk, const CUtensorMap& tq) {
+  static_assert(sizeof(Smem<G>) + 1024 <= 227 * 1024, "indexer shared memory exceeds 227 KB");
   const size_t smem = sizeof(Smem<G>) + 1024;
   auto fn = indexer_kernel<G>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
