@@ -432,10 +432,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < G; ++j) {
           float v[64];
           tmem_ld64_sync(taddr + j * 64, v);
-          float acc = 0.f;
+          // four partial sums: a single 64-long FMA chain is latency bound
+          float a4[4] = {0.f, 0.f, 0.f, 0.f};
           const float* wj = s.wq[slot] + j * 64;
 #pragma unroll
-          for (int h = 0; h < 64; ++h) acc = fmaf(wj[h], fmaxf(v[h], 0.f), acc);
+          for (int h = 0; h < 64; ++h) a4[h & 3] = fmaf(wj[h], fmaxf(v[h], 0.f), a4[h & 3]);
+          const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
           if (j < nr && tok < cur.row_len(j) && tok < p.ld)
             p.logits[static_cast<int64_t>(r0 + j) * p.ld + tok] = acc * sc;
         }
