@@ -1,41 +1,43 @@
 // Exact per-row top-k (the fine-grained token selection of Eq. (2), "DeepSeek
 // V3.2-Exp support", section "1. Architecture").
 //
-// Each row is owned by one thread-block cluster of kC CTAs; CTA c takes the
-// c-th contiguous slice of the row.  Histograms are merged across the cluster
-// through distributed shared memory, so the row is read from HBM once and the
-// later passes run on shared memory.  Clusters loop over rows (persistent).
+// One CTA of 1024 threads owns a row (persistent over rows, one CTA per SM).
+// Every pass synchronises with __syncthreads only: measured on GB300, one such
+// CTA streams a 512 KB row in ~6 us, while the cross-CTA histogram merges of a
+// cluster-per-row design cost ~2-3 us per radix pass.
 //
-// Selection is a most-significant-digit radix select (8-bit digits) on the
+// Selection is a most-significant-digit radix select (11-bit digits) on the
 // 64-bit key  (order-preserving u32 of the f32 score) << 32 | ~column,  which
 // is unique per element: the k largest keys are the k best scores with ties
 // going to the lower column.  It stops as soon as the bin holding the k-th key
 // is taken whole, so the column digits are only visited for real ties.
 //
-//  * full-row path (shorter rows): the slice's keys are staged in shared
-//    memory and the radix select runs over all of them;
-//  * cutoff path (long rows; the "sampled filtering" of vLLM's persistent
-//    top-k in the RepoJournal digest): a strided sample of the row gives a
-//    cutoff tau expected to keep about 2k elements; one streaming pass
-//    compacts the survivors (key >= tau) into shared memory; the exact radix
-//    select then runs on the survivors only.  If the estimate missed (fewer
-//    than k survivors, or more than fit) the row is redone by the full-row
-//    radix reading global memory, so the result is always exact.
-#include <cooperative_groups.h>
-
+//  * staged path (rows up to kStage scores): the row's keys are staged in
+//    shared memory and the radix select runs over all of them;
+//  * cutoff path (longer rows; the "sampled filtering" of vLLM's persistent
+//    top-k in the RepoJournal digest): a sample of the row (runs of 8 scores
+//    spread over it) gives a cutoff tau expected to keep about 2k elements;
+//    one streaming pass compacts the survivors (key >= tau) into shared
+//    memory; the exact select then runs on the survivors only (its first
+//    digit linear in the key over [tau, largest survivor]).  If the
+//    estimate missed (fewer than k survivors, or more than fit) the row is
+//    redone by the radix select reading the row from global memory, so the
+//    result is always exact.
 #include "internal.h"
 #include "ptx.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace dsa {
 namespace {
 
-constexpr int kC = 8;       // CTAs per row (cluster size, portable)
-constexpr int kT = 256;     // threads per CTA
-constexpr int kCap = 8192;  // u32 slots per CTA: staged keys, or survivor (key, column) pairs
-constexpr int kPairCap = kCap / 2;
-constexpr int kSample = 256;  // sample elements per CTA (cutoff path)
+constexpr int kT = 1024;                // threads per CTA
+constexpr int kWarps = kT / 32;
+constexpr int kStage = 40960;           // u32 slots: staged keys, or survivor pairs
+constexpr int kWarpCap = kStage / 2 / kWarps;  // survivor pairs per warp (640)
+// Cutoff-path sample: kGroups runs of 8 consecutive scores spread evenly over
+// the row (one 32-byte sector each).
+constexpr int kGroups = 256;
+constexpr int kSample = 8 * kGroups;
+static_assert(kSample / 4 <= kT, "the sample is loaded as one float4 per thread");
 
 struct TkParams {
   const float* logits;
@@ -52,14 +54,16 @@ struct TkParams {
 };
 
 struct TkSmem {
-  uint32_t data[kCap];
+  uint32_t data[kStage];  // staged keys | survivor keys (warp regions) + columns
   uint32_t sample[kSample];
-  uint32_t hist[256];
-  uint32_t chist[2][256];  // read by the other CTAs of the cluster
-  uint32_t counter;        // rank 0's is the cluster-wide output cursor
-  uint32_t cnt;            // survivors of this CTA (cluster-visible)
-  uint32_t overflow;       // cluster-visible
+  uint32_t hist[2048];    // radix histogram (kBins)
+  uint32_t wscan[kWarps]; // per-warp scan totals
+  uint32_t wsum[kWarps];  // per-warp survivor counts
+  uint32_t wmax[kWarps];  // per-warp largest survivor key
+  uint32_t counter;       // output cursor
   uint32_t bin, above, binc;
+  uint32_t ncand;         // candidates gathered from the boundary bin
+  uint64_t thr;           // the select's result
 };
 
 __device__ __forceinline__ uint32_t key_of(float x) {
@@ -68,75 +72,98 @@ __device__ __forceinline__ uint32_t key_of(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Radix state: after `depth` digits the selected set is every element whose
-// top `depth` digits of (key, ~col) are >= (phi, plo).
+// Radix state: the selected set is every element whose top kb bits of key and
+// (once kb == 32) top ib bits of ~column are >= (phi, plo).  Digits are up to
+// kDigit bits wide; key digits may start at any bit (the survivor select
+// starts at the highest bit where the survivors differ).
+constexpr int kDigit = 11;
+constexpr int kBins = 1 << kDigit;
 struct Sel {
-  int depth;
+  int kb, ib;
   uint32_t phi, plo;
 };
 
 __device__ __forceinline__ bool matches(const Sel& s, uint32_t key, uint32_t nidx) {
-  const int d = s.depth;
-  if (d == 0) return true;
-  if (d < 4) return (key >> (32 - 8 * d)) == s.phi;
+  if (s.kb < 32) return s.kb == 0 || (key >> (32 - s.kb)) == s.phi;
   if (key != s.phi) return false;
-  if (d == 4) return true;
-  return (nidx >> (32 - 8 * (d - 4))) == s.plo;
+  return s.ib == 0 || (nidx >> (32 - s.ib)) == s.plo;
 }
 
-__device__ __forceinline__ uint32_t digit(int d, uint32_t key, uint32_t nidx) {
-  return d < 4 ? (key >> (24 - 8 * d)) & 255u : (nidx >> (24 - 8 * (d - 4))) & 255u;
+// Width of the next digit, and the digit itself.
+__device__ __forceinline__ int digit_bits(const Sel& s) {
+  return min(kDigit, 32 - (s.kb < 32 ? s.kb : s.ib));
+}
+__device__ __forceinline__ uint32_t digit(const Sel& s, int w, uint32_t key, uint32_t nidx) {
+  return s.kb < 32 ? (key >> (32 - s.kb - w)) & ((1u << w) - 1u)
+                   : (nidx >> (32 - s.ib - w)) & ((1u << w) - 1u);
 }
 
-__device__ __forceinline__ bool selected(const Sel& s, uint32_t key, uint32_t nidx) {
-  const int d = s.depth;
-  if (d < 4) return (key >> (32 - 8 * d)) >= s.phi;
-  if (d == 4) return key >= s.phi;
-  if (key != s.phi) return key > s.phi;
-  return (nidx >> (32 - 8 * (d - 4))) >= s.plo;
+// The smallest 64-bit (key, ~column) value whose leading fixed bits equal the
+// state's prefix: once the select is done, the selected set is exactly the
+// elements whose (key << 32 | ~column) is >= this threshold.
+__device__ __forceinline__ uint64_t threshold(const Sel& s) {
+  const uint32_t hi = s.kb == 0 ? 0u : (s.kb == 32 ? s.phi : s.phi << (32 - s.kb));
+  const uint32_t lo = s.ib == 0 ? 0u : (s.ib == 32 ? s.plo : s.plo << (32 - s.ib));
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t pack(uint32_t key, uint32_t nidx) {
+  return (static_cast<uint64_t>(key) << 32) | nidx;
 }
 
-// Warp-aggregated histogram increment (all 32 lanes call it).
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool valid) {
-  const unsigned act = __ballot_sync(0xffffffffu, valid);
-  if (valid) {
-    const unsigned peers = __match_any_sync(act, bin);
-    if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(peers) - 1))
-      atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
-  }
+// Read-only global loads as volatile asm: they are issued in program order, so
+// a batch of them is in flight before the first one is consumed.
+__device__ __forceinline__ float4 ldg_nc4(const float* ptr) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ float ldg_nc(const float* ptr) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+  return v;
 }
 
-// Element sources.  visit(f) calls f(key, ~col, valid) with every lane of
-// every warp taking part in each call (valid = false for padding lanes).
-struct SrcGlobal {  // the slice [lo, hi) of a row, read from global memory
+// Element sources.  visit(f) calls f(key, ~col, valid) with every lane of a
+// warp taking part in each call (valid = false for padding lanes).
+
+struct SrcGlobal {  // the row [0, n), read from global memory
   const float* row;
-  int lo, hi;
+  int n;
+  static constexpr int kB = 4;  // float4 loads in flight per thread
+  __device__ float4 load4(int e0) const {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e0 + 3 < n) {
+      v = ldg_nc4(row + e0);
+    } else if (e0 < n) {
+      v.x = row[e0];
+      if (e0 + 1 < n) v.y = row[e0 + 1];
+      if (e0 + 2 < n) v.z = row[e0 + 2];
+    }
+    return v;
+  }
   template <class F>
   __device__ void visit(F&& f) const {
-    const int n = hi - lo;
     const int n4 = (n + 3) >> 2;
-    const int lim = ((n4 + kT - 1) / kT) * kT;
-    for (int i4 = threadIdx.x; i4 < lim; i4 += kT) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int e0 = 4 * i4;
-      if (e0 + 3 < n) {
-        v = *reinterpret_cast<const float4*>(row + lo + e0);
-      } else if (e0 < n) {
-        v.x = row[lo + e0];
-        if (e0 + 1 < n) v.y = row[lo + e0 + 1];
-        if (e0 + 2 < n) v.z = row[lo + e0 + 2];
-      }
-      const float vv[4] = {v.x, v.y, v.z, v.w};
+    for (int base = 0; base < n4; base += kB * kT) {  // same trip count in every thread
+      float4 v[kB];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        f(key_of(vv[j]), ~static_cast<uint32_t>(lo + e0 + j), e0 + j < n);
+      for (int b = 0; b < kB; ++b) v[b] = load4(4 * (base + b * kT + threadIdx.x));
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int e0 = 4 * (base + b * kT + threadIdx.x);
+        const float vv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f(key_of(vv[j]), ~static_cast<uint32_t>(e0 + j), e0 + j < n);
+      }
     }
   }
 };
 
-struct SrcStaged {  // keys of the slice staged in shared memory, in column order
+struct SrcStaged {  // the row's keys staged in shared memory, in column order
   const uint32_t* keys;
-  int lo, n;
+  int n;
   template <class F>
   __device__ void visit(F&& f) const {
     const int n4 = (n + 3) >> 2;
@@ -147,108 +174,284 @@ struct SrcStaged {  // keys of the slice staged in shared memory, in column orde
       if (e0 < n) v = *reinterpret_cast<const uint4*>(keys + e0);
       const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) f(vv[j], ~static_cast<uint32_t>(lo + e0 + j), e0 + j < n);
+      for (int j = 0; j < 4; ++j) f(vv[j], ~static_cast<uint32_t>(e0 + j), e0 + j < n);
     }
   }
 };
 
-struct SrcPairs {  // survivors: keys[i] at column cols[i]
+struct SrcPairs {  // survivors: warp w's are keys/cols [w*kWarpCap, w*kWarpCap + cnt[w])
   const uint32_t* keys;
   const uint32_t* cols;
-  int n;
+  const uint32_t* cnt;
   template <class F>
   __device__ void visit(F&& f) const {
-    const int lim = ((n + kT - 1) / kT) * kT;
-    for (int i = threadIdx.x; i < lim; i += kT) {
+    const int lane = threadIdx.x & 31;
+    const int w0 = (threadIdx.x >> 5) * kWarpCap;  // each warp walks its own region
+    const int n = static_cast<int>(min(cnt[threadIdx.x >> 5], static_cast<uint32_t>(kWarpCap)));
+    const int lim = (n + 31) & ~31;
+    for (int i = lane; i < lim; i += 32) {
       const bool ok = i < n;
-      f(ok ? keys[i] : 0u, ok ? ~cols[i] : 0u, ok);
+      f(ok ? keys[w0 + i] : 0u, ok ? ~cols[w0 + i] : 0u, ok);
     }
   }
 };
 
-struct SrcKeys {  // a key-only list (the sample)
-  const uint32_t* keys;
-  int n;
-  template <class F>
-  __device__ void visit(F&& f) const {
-    const int lim = ((n + kT - 1) / kT) * kT;
-    for (int i = threadIdx.x; i < lim; i += kT) {
-      const bool ok = i < n;
-      f(ok ? keys[i] : 0u, 0u, ok);
+// One histogram pass: bin(key, ~col) gives each element's bin in [0, kBins)
+// or -1 for elements outside the current selection.  Leaves in s.bin the bin
+// holding the need-th largest element (counting bins from the top), in
+// s.above the elements of the higher bins and in s.binc the bin's own count.
+// Histogram increments are plain shared-memory atomics: measured on GB300
+// over 2048 normal scores, a 256-bin pass costs ~0.6-0.9 k cycles this way
+// against 3-13 k cycles when equal bins are first combined with
+// __match_any_sync.
+template <class Src, class Bin>
+__device__ void hist_pass(const Src& src, const Bin& bin, uint32_t need, TkSmem& s) {
+  constexpr int kPer = kBins / kT;  // bins per thread in the scan
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kBins; i += kT) s.hist[i] = 0;
+  __syncthreads();
+  src.visit([&](uint32_t key, uint32_t nidx, bool valid) {
+    const int b = valid ? bin(key, nidx) : -1;
+    if (b >= 0) atomicAdd(&s.hist[b], 1u);
+  });
+  __syncthreads();
+  // thread t owns bins [kBins - kPer*(t+1), kBins - kPer*t), walked downwards
+  const int top = kBins - kPer * tid - 1;
+  uint32_t h[kPer], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    h[j] = s.hist[top - j];
+    sum += h[j];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s.wscan[warp] = incl;
+  __syncthreads();
+  const uint32_t wt = s.wscan[lane];
+  uint32_t wincl = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += v;
+  }
+  uint32_t above = __shfl_sync(0xffffffffu, wincl - wt, warp) + incl - sum;
+  if (above < need && need <= above + sum) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (above + h[j] >= need) {
+        s.bin = static_cast<uint32_t>(top - j);
+        s.above = above;
+        s.binc = h[j];
+        break;
+      }
+      above += h[j];
     }
   }
-};
+  if (tid == 0) s.ncand = 0;
+  __syncthreads();
+}
 
-// Cluster-wide radix select: returns the state whose selected set has exactly
-// `need` elements over the union of the CTAs' sources (for key-only sources
-// with ties at the last digit: the smallest key with at least `need` elements
-// at or above it).  `phase` counts passes for the double-buffered cluster
-// histograms and advances identically in every CTA of the cluster.
+constexpr uint32_t kCandCap = 512;  // boundary-bin elements ranked directly
+static_assert(2 * kCandCap <= kSample, "the candidate list aliases the sample");
+
+// Gathers the n elements with in_bin(key, ~col) (n <= kCandCap) and returns the
+// (key, ~col) value of the need-th largest of them (keys are unique, so
+// exactly one has rank need - 1).
+template <class Src, class In>
+__device__ uint64_t rank_finish(const Src& src, const In& in_bin, uint32_t n, uint32_t need,
+                                TkSmem& s) {
+  uint64_t* cand = reinterpret_cast<uint64_t*>(s.sample);  // free once tau is known
+  src.visit([&](uint32_t key, uint32_t nidx, bool valid) {
+    if (valid && in_bin(key, nidx)) cand[atomicAdd(&s.ncand, 1u)] = pack(key, nidx);
+  });
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < n; i += kT) {
+    const uint64_t c = cand[i];
+    uint32_t r = 0;
+    for (uint32_t j = 0; j < n; ++j) r += cand[j] > c ? 1u : 0u;
+    if (r == need - 1) s.thr = c;
+  }
+  __syncthreads();
+  const uint64_t thr = s.thr;
+  __syncthreads();
+  return thr;
+}
+
+// Radix select from the state `st`: returns the threshold whose selected set
+// (elements with (key << 32 | ~col) >= it) has exactly `need` elements over
+// the source.  Digits are taken from the top; once the bin holding the
+// need-th element has few enough elements they are ranked directly.
 template <class Src>
-__device__ Sel cluster_select(const Src& src, uint32_t need, int max_depth, TkSmem& s,
-                              cg::cluster_group& cluster, int& phase) {
-  Sel st{0, 0u, 0u};
-  const int tid = threadIdx.x;
-  while (st.depth < max_depth) {
-    if (tid < 256) s.hist[tid] = 0;
-    __syncthreads();
-    const int d = st.depth;
-    src.visit([&](uint32_t key, uint32_t nidx, bool valid) {
-      const bool m = valid && matches(st, key, nidx);
-      hist_add(s.hist, digit(d, key, nidx), m);
-    });
-    __syncthreads();
-    const int buf = phase & 1;
-    ++phase;
-    if (tid < 256) s.chist[buf][tid] = s.hist[tid];
-    cluster.sync();
-    if (tid < 256) {
-      uint32_t tot = 0;
-#pragma unroll
-      for (int r = 0; r < kC; ++r) tot += cluster.map_shared_rank(&s.chist[buf][0], r)[tid];
-      s.hist[tid] = tot;
-    }
-    __syncthreads();
-    if (tid < 32) {
-      // lane l owns bins 255-8l .. 248-8l (descending)
-      const int lane = tid;
-      uint32_t h[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        h[j] = s.hist[255 - 8 * lane - j];
-        sum += h[j];
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      uint32_t above = incl - sum;
-      if (above < need && need <= incl) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (above + h[j] >= need) {
-            s.bin = 255 - 8 * lane - j;
-            s.above = above;
-            s.binc = h[j];
-            break;
-          }
-          above += h[j];
-        }
-      }
-    }
-    __syncthreads();
-    const uint32_t b = s.bin;
+__device__ uint64_t radix_select(const Src& src, uint32_t need, Sel st, TkSmem& s) {
+  for (;;) {
+    const int w = digit_bits(st);
+    hist_pass(src, [&](uint32_t key, uint32_t nidx) {
+      return matches(st, key, nidx) ? static_cast<int>(digit(st, w, key, nidx)) : -1;
+    }, need, s);
+    const uint32_t b = s.bin, binc = s.binc;
     need -= s.above;
-    if (d < 4) st.phi = (st.phi << 8) | b;
-    else st.plo = (st.plo << 8) | b;
-    st.depth = d + 1;
-    const bool done = s.binc == need;
+    if (st.kb < 32) {
+      st.phi = st.kb == 0 ? b : (st.phi << w) | b;
+      st.kb += w;
+    } else {
+      st.plo = st.ib == 0 ? b : (st.plo << w) | b;
+      st.ib += w;
+    }
+    if (binc == need) return threshold(st);  // the boundary bin is taken whole
+    if (binc <= kCandCap)
+      return rank_finish(src, [&](uint32_t key, uint32_t nidx) { return matches(st, key, nidx); },
+                         binc, need, s);
     __syncthreads();
-    if (done) break;
   }
-  return st;
+}
+
+// Select over the survivors of the cutoff path, whose keys all lie in
+// [tau, kmax]: the first digit is linear in the key, (key - tau) >> shift over
+// kBins bins, so the survivors spread evenly over the bins even when their
+// range crosses an exponent boundary (where a leading-bits digit would put
+// most of them in one bin).  Heavy ties fall back to the leading-bits radix.
+template <class Src>
+__device__ uint64_t survivor_select(const Src& src, uint32_t need, uint32_t tau, uint32_t kmax,
+                                    TkSmem& s) {
+  const uint32_t span = kmax - tau;
+  const int shift = span < static_cast<uint32_t>(kBins) ? 0 : 32 - kDigit - __clz(span);
+  hist_pass(src, [&](uint32_t key, uint32_t) {
+    return key >= tau ? static_cast<int>((key - tau) >> shift) : -1;
+  }, need, s);
+  const uint32_t b = s.bin, binc = s.binc;
+  const uint32_t rest = need - s.above;
+  if (binc <= kCandCap)
+    return rank_finish(src, [&](uint32_t key, uint32_t) {
+      return key >= tau && ((key - tau) >> shift) == b;
+    }, binc, rest, s);
+  __syncthreads();
+  const uint32_t x = tau ^ kmax;
+  const int nb = x == 0 ? 32 : __clz(x);
+  const Sel st0{nb, 0, nb == 0 ? 0u : (nb == 32 ? kmax : kmax >> (32 - nb)), 0u};
+  return radix_select(src, need, st0, s);
+}
+
+// Cutoff estimate: the lower edge of the 12-bit key prefix (sign, exponent,
+// 3 mantissa bits) bin that holds the q-th largest of the n sample keys, from
+// one 4096-bin histogram in `bins` (shared memory) and a block scan from the
+// top bin down.  Keeping every key >= that edge keeps at least q / n of the
+// row in expectation.
+__device__ uint32_t local_tau(const uint32_t* sample, int n, uint32_t q, uint32_t* bins,
+                              TkSmem& s) {
+  constexpr int kTauBins = 4096, kPer = kTauBins / kT;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kTauBins; i += kT) bins[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kT) atomicAdd(&bins[sample[i] >> 20], 1u);
+  __syncthreads();
+  // thread t owns bins [kTauBins - kPer*(t+1), kTauBins - kPer*t), walked downwards
+  const int top = kTauBins - kPer * tid - 1;
+  uint32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) sum += bins[top - j];
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s.wscan[warp] = incl;
+  __syncthreads();
+  uint32_t above = incl - sum;
+  for (int w = 0; w < warp; ++w) above += s.wscan[w];
+  if (above < q && q <= above + sum) {
+    for (int j = 0; j < kPer; ++j) {
+      above += bins[top - j];
+      if (above >= q) {
+        s.bin = static_cast<uint32_t>(top - j);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t tau = s.bin << 20;
+  __syncthreads();
+  return tau;
+}
+
+// One streaming pass over the row: every element with key >= tau goes to its
+// warp's region of (keys, cols) (warp w owns [w*kWarpCap, (w+1)*kWarpCap) and
+// keeps its running count in a register, so the pass takes no atomics).
+// s.wsum[w] receives the warp's count (it may exceed kWarpCap: the caller
+// then treats the row as overflowed) and s.wmax[w] its largest kept key (0 if
+// none).  For tau above key(+0.0), key_of(x) >= tau is exactly the signed
+// compare of x's bits with tau's float bits (negative values, -0.0 and -NaN
+// fall below, +NaN above, as in key_of): one instruction per element.
+template <bool kPositiveTau>
+__device__ void compact(const SrcGlobal& g, uint32_t tau, uint32_t* keys, uint32_t* cols,
+                        TkSmem& s) {
+  constexpr int kB = 4;  // float4 loads per batch
+  const int n = g.n;
+  const int n4 = (n + 3) >> 2;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint32_t* wkeys = keys + warp * kWarpCap;
+  uint32_t* wcols = cols + warp * kWarpCap;
+  const int32_t tbits = static_cast<int32_t>(tau & 0x7fffffffu);
+  uint32_t kmax = 0, wcount = 0;
+  for (int base = 0; base < n4; base += kB * kT) {
+    float4 v[kB];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) v[b] = g.load4(4 * (base + b * kT + threadIdx.x));
+    uint32_t mask = 0;  // bit 4b + j: element j of load b is kept
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const float vv[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool keep = kPositiveTau ? static_cast<int32_t>(__float_as_uint(vv[j])) >= tbits
+                                       : key_of(vv[j]) >= tau;
+        mask |= (keep ? 1u : 0u) << (4 * b + j);
+      }
+    }
+    if (4 * (base + kB * kT) > n) {  // the last batch: drop the elements past the row
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int e0 = 4 * (base + b * kT + threadIdx.x);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (e0 + j >= n) mask &= ~(1u << (4 * b + j));
+      }
+    }
+    const uint32_t c = __popc(mask);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+    // survivors are few: walk the set bits, re-reading each kept score (an L1
+    // hit) rather than selecting it from the registers by a dynamic index
+    uint32_t pos = wcount + incl - c;
+    while (mask != 0) {
+      const int bit = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int e = 4 * (base + (bit >> 2) * kT + threadIdx.x) + (bit & 3);
+      const uint32_t key = key_of(ldg_nc(g.row + e));
+      kmax = max(kmax, key);
+      if (pos < static_cast<uint32_t>(kWarpCap)) {
+        wkeys[pos] = key;
+        wcols[pos] = static_cast<uint32_t>(e);
+      }
+      ++pos;
+    }
+    wcount += wtot;
+  }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    s.wsum[warp] = wcount;
+    s.wmax[warp] = kmax;
+  }
 }
 
 __device__ __forceinline__ int32_t map_col(const TkParams& p, int row, uint32_t col) {
@@ -263,17 +466,15 @@ __device__ __forceinline__ int32_t map_col(const TkParams& p, int row, uint32_t 
 
 // Writes every selected element of the source to out[row], in any order.
 template <class Src>
-__device__ void emit(const Src& src, const Sel& st, const TkParams& p, int row, TkSmem& s,
-                     cg::cluster_group& cluster) {
-  uint32_t* cursor = cluster.map_shared_rank(&s.counter, 0);
+__device__ void emit(const Src& src, uint64_t thr, const TkParams& p, int row, TkSmem& s) {
   int32_t* out = p.out + static_cast<int64_t>(row) * p.k;
   const int lane = threadIdx.x & 31;
   src.visit([&](uint32_t key, uint32_t nidx, bool valid) {
-    const bool take = valid && selected(st, key, nidx);
+    const bool take = valid && pack(key, nidx) >= thr;
     const unsigned m = __ballot_sync(0xffffffffu, take);
     if (m == 0) return;
     uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(cursor, static_cast<uint32_t>(__popc(m)));
+    if (lane == 0) base = atomicAdd(&s.counter, static_cast<uint32_t>(__popc(m)));
     base = __shfl_sync(0xffffffffu, base, 0);
     if (take) {
       const uint32_t pos = base + __popc(m & ((1u << lane) - 1u));
@@ -282,131 +483,106 @@ __device__ void emit(const Src& src, const Sel& st, const TkParams& p, int row, 
   });
 }
 
-__global__ void __launch_bounds__(kT, 4) topk_kernel(const TkParams p) {
+__global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
   extern __shared__ uint8_t smem_raw[];
   TkSmem& s =
       *reinterpret_cast<TkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int cid = blockIdx.x / kC;
-  const int ncl = gridDim.x / kC;
   const int tid = threadIdx.x;
-  int phase = 0;
 
-  for (int row = cid; row < p.R; row += ncl) {
+  for (int row = blockIdx.x; row < p.R; row += gridDim.x) {
     const float* rowp = p.logits + static_cast<int64_t>(row) * p.ld;
     int L = p.row_len[row];
     if (L < 0) L = 0;
     if (L > p.ld) {
-      if (tid == 0 && rank == 0) raise_error(p.err, kErrBadIndex);
+      if (tid == 0) raise_error(p.err, kErrBadIndex);
       L = static_cast<int>(p.ld);
     }
-    const int S = (((L + kC - 1) / kC) + 3) & ~3;
-    const int lo = min(L, rank * S);
-    const int hi = min(L, lo + S);
     int32_t* out = p.out + static_cast<int64_t>(row) * p.k;
 
     if (L <= p.k) {
-      // every column is selected; the tail is -1 (no cluster communication)
-      for (int c = lo + tid; c < hi; c += kT) out[c] = map_col(p, row, c);
-      const int pad = p.k - L;
-      const int per = (pad + kC - 1) / kC;
-      const int a = L + rank * per, b = min(p.k, a + per);
-      for (int c = a + tid; c < b; c += kT) out[c] = -1;
+      // every column is selected; the tail is -1
+      for (int c = tid; c < p.k; c += kT) out[c] = c < L ? map_col(p, row, c) : -1;
       continue;
     }
 
-    if (tid == 0) {
-      s.counter = 0;
-      s.overflow = 0;
-      s.cnt = 0;
-    }
-    const bool cutoff =
-        p.force_path == 2 || (p.force_path == 0 && L >= (p.k < 1024 ? 98304 : 65536));
-    cluster.sync();  // counters reset everywhere before anyone emits
-
+    if (tid == 0) s.counter = 0;
+    __syncthreads();
+    const bool cutoff = p.force_path == 2 || (p.force_path == 0 && L > kStage);
     bool done = false;
     if (cutoff) {
-      // 1. sample -> cutoff tau expected to keep about 2k elements
-      const int n = hi - lo;
-      const int ns = min(kSample, n);
-      const int stride = ns > 0 ? n / ns : 1;
-      for (int i = tid; i < ns; i += kT) s.sample[i] = key_of(rowp[lo + i * stride]);
-      __syncthreads();
-      int NS = 0;
-      for (int r = 0; r < kC; ++r) {
-        const int lr = min(L, r * S), hr = min(L, lr + S);
-        NS += min(kSample, hr - lr);
+      // 1. the row's sample -> cutoff tau expected to keep about 2k elements.
+      // Rows shorter than the sample are taken whole.
+      int ns;
+      if (L >= kSample) {
+        ns = kSample;
+        if (tid < kSample / 4) {
+          // float4 tid of the sample: group tid / 2, half tid % 2
+          const int64_t g0 =
+              ((static_cast<int64_t>(tid >> 1) * (L - 8)) / (kGroups - 1)) & ~3ll;
+          const float4 v = ldg_nc4(rowp + g0 + 4 * (tid & 1));
+          *reinterpret_cast<uint4*>(s.sample + 4 * tid) =
+              make_uint4(key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w));
+        }
+      } else {
+        ns = L;
+        for (int i = tid; i < L; i += kT) s.sample[i] = key_of(ldg_nc(rowp + i));
       }
-      const double want = 2.0 * p.k * static_cast<double>(NS) / static_cast<double>(L);
-      const uint32_t q = static_cast<uint32_t>(fmin(static_cast<double>(NS), ceil(want)));
-      SrcKeys sk{s.sample, ns};
-      // two digits (sign, exponent, 7 mantissa bits) place tau within ~1 % of
-      // the sample's q-th key, which is all the estimate needs
-      const Sel ts = cluster_select(sk, q > 0 ? q : 1u, 2, s, cluster, phase);
-      const uint32_t tau = ts.phi << (32 - 8 * ts.depth);
+      __syncthreads();
+      // q = ceil(2k ns / L) sample keys above tau (integer arithmetic: FP64 is
+      // a slow pipe on GB300 and every thread evaluates this)
+      const int64_t want = (2 * static_cast<int64_t>(p.k) * ns + L - 1) / L;
+      const uint32_t q = static_cast<uint32_t>(want < ns ? want : ns);
+      // the survivor area is free until the compaction: it holds the bins
+      const uint32_t tau = local_tau(s.sample, ns, q > 0 ? q : 1u, s.data, s);
       // 2. one streaming pass: compact the survivors (key >= tau)
       uint32_t* skeys = s.data;
-      uint32_t* scols = s.data + kPairCap;
-      SrcGlobal g{rowp, lo, hi};
-      const int lane = tid & 31;
-      g.visit([&](uint32_t key, uint32_t nidx, bool valid) {
-        const bool keep = valid && key >= tau;
-        const unsigned m = __ballot_sync(0xffffffffu, keep);
-        if (m == 0) return;
-        uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(&s.cnt, static_cast<uint32_t>(__popc(m)));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (keep) {
-          const uint32_t pos = base + __popc(m & ((1u << lane) - 1u));
-          if (pos < kPairCap) {
-            skeys[pos] = key;
-            scols[pos] = ~nidx;
-          }
-        }
-      });
+      uint32_t* scols = s.data + kWarps * kWarpCap;
+      const SrcGlobal g{rowp, L};
+      if (tau > 0x80000000u) compact<true>(g, tau, skeys, scols, s);
+      else compact<false>(g, tau, skeys, scols, s);
       __syncthreads();
-      if (tid == 0 && s.cnt > kPairCap) s.overflow = 1;
-      cluster.sync();
-      uint32_t total = 0, over = 0;
-      for (int r = 0; r < kC; ++r) {
-        total += *cluster.map_shared_rank(&s.cnt, r);
-        over |= *cluster.map_shared_rank(&s.overflow, r);
+      uint32_t total = 0, cmax = 0;
+      bool over = false;
+#pragma unroll 8
+      for (int w = 0; w < kWarps; ++w) {
+        total += s.wsum[w];
+        over |= s.wsum[w] > static_cast<uint32_t>(kWarpCap);
+        cmax = max(cmax, s.wmax[w]);
       }
       if (!over && total >= static_cast<uint32_t>(p.k)) {
-        SrcPairs sp{skeys, scols, static_cast<int>(min(s.cnt, static_cast<uint32_t>(kPairCap)))};
-        const Sel st = cluster_select(sp, p.k, 8, s, cluster, phase);
-        emit(sp, st, p, row, s, cluster);
+        const SrcPairs sp{skeys, scols, s.wsum};
+        static_assert(kBins % kT == 0 && kBins <= 2048, "hist holds kBins bins");
+        const uint64_t thr = survivor_select(sp, p.k, tau, cmax, s);
+        emit(sp, thr, p, row, s);
         done = true;
-      } else if (tid == 0 && rank == 0) {
+      } else if (tid == 0) {
         raise_error(p.err, kErrCapacity);
       }
     }
     if (!done) {
-      const int n = hi - lo;
       // full-row radix select (also the exact redo of a missed cutoff)
-      if (!cutoff && n <= kCap) {
-        for (int i4 = tid; 4 * i4 < n; i4 += kT) {
+      if (!cutoff && L <= kStage) {
+        for (int i4 = tid; 4 * i4 < L; i4 += kT) {
           const int e0 = 4 * i4;
-          if (e0 + 3 < n) {
-            const float4 v = *reinterpret_cast<const float4*>(rowp + lo + e0);
+          if (e0 + 3 < L) {
+            const float4 v = ldg_nc4(rowp + e0);
             *reinterpret_cast<uint4*>(s.data + e0) =
                 make_uint4(key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w));
           } else {
-            for (int j = e0; j < n; ++j) s.data[j] = key_of(rowp[lo + j]);
+            for (int j = e0; j < L; ++j) s.data[j] = key_of(rowp[j]);
           }
         }
         __syncthreads();
-        SrcStaged ss{s.data, lo, n};
-        const Sel st = cluster_select(ss, p.k, 8, s, cluster, phase);
-        emit(ss, st, p, row, s, cluster);
+        const SrcStaged ss{s.data, L};
+        const uint64_t thr = radix_select(ss, p.k, Sel{0, 0, 0u, 0u}, s);
+        emit(ss, thr, p, row, s);
       } else {
-        SrcGlobal g{rowp, lo, hi};
-        const Sel st = cluster_select(g, p.k, 8, s, cluster, phase);
-        emit(g, st, p, row, s, cluster);
+        const SrcGlobal g{rowp, L};
+        const uint64_t thr = radix_select(g, p.k, Sel{0, 0, 0u, 0u}, s);
+        emit(g, thr, p, row, s);
       }
     }
-    cluster.sync();  // all emits done before the counters are reused
+    __syncthreads();  // all emits done before the counter and the buffers are reused
   }
 }
 
@@ -419,25 +595,9 @@ cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t s
   if (e != cudaSuccess) return e;
   TkParams p{a.logits, a.ld,  a.row_len, a.R,          a.k,          a.col_blocks,
              a.nb,     a.block_size, a.out, a.force_path, dev.err_word};
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kC;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kT);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int max_clusters = 0;
-  cfg.gridDim = dim3(kC * 64);
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, topk_kernel, &cfg);
-  if (e != cudaSuccess) return e;
-  if (max_clusters < 1) max_clusters = 1;
-  const int ncl = a.R < max_clusters ? a.R : max_clusters;
-  cfg.gridDim = dim3(kC * ncl);
-  return cudaLaunchKernelEx(&cfg, topk_kernel, p);
+  const int grid = a.R < dev.sm_count ? a.R : dev.sm_count;
+  topk_kernel<<<grid, kT, smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace dsa

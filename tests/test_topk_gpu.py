@@ -73,3 +73,22 @@ def test_topk_column_map():
     ref = oracle.topk(np_(logits).astype(np.float64), np_(L), 256, col_blocks=np_(blocks), bs=bs)
     for i in range(R):
         assert sorted(np_(sel)[i].tolist()) == sorted(ref[i].tolist())
+
+
+def test_topk_cutoff_at_or_below_zero():
+    """Rows whose k-th largest score is negative or a (signed) zero, so the
+    sampled cutoff of the long-row path is at or below +0.0; with positive
+    cutoffs the compaction compares raw float bits instead of ordered keys."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    ld = 131072
+    L = torch.tensor([131072, 131072, 100003], dtype=torch.int32, device="cuda")
+    logits = -torch.randn(3, ld, generator=g, device="cuda").abs()
+    # row 1: 1000 positive scores, then 3000 zeros of both signs around the k-th
+    logits[1, :1000] = torch.rand(1000, generator=g, device="cuda") + 0.5
+    logits[1, 5000:6500] = 0.0
+    logits[1, 6500:8000] = -0.0
+    # row 2: negative scores only, with many exact ties
+    logits[2] = -torch.randint(1, 50, (ld,), generator=g, device="cuda").float()
+    for force in (0, 2):
+        sel = gpu_topk(logits, ld, L, 2048, force_path=force)
+        sets_equal(sel, logits, L, 2048)
