@@ -89,6 +89,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+
+// 2^x by the hardware approximation (a few ulp; P is rounded to bf16 anyway).
+// 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -320,33 +328,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) m[u] = __ballot_sync(0xffffffffu, sel[u] >= 0);
       load_sel(i + 1, sel);
+      const bool all_valid = (m[0] & m[1] & m[2] & m[3]) == 0xffffffffu;  // warp-uniform
       const int buf = i & 1;
       if (!mbar_wait_warp(&s.s_full[buf], (i >> 1) & 1, p.err, abort)) { bad = true; break; }
       tc_fence_after();
       const uint32_t sbase = lane_base + kSCol + buf * kTile;
-      // scores of tokens j (column j of the tile) in log2 units, -inf if skipped
-      auto scaled = [&](float (&v)[64], int half) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int t = 64 * half + j;
-          const bool ok = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
-          v[j] = ok ? v[j] * p.scale_log2 : -INFINITY;
-        }
-      };
-      float mt = -INFINITY;
+      // One pass over the tile's scores (log2 units, -inf if skipped), 64
+      // columns at a time.  P = 2^(x - m_t) against the running reference m_t,
+      // which only moves when a score exceeds it by more than the threshold
+      // (then P already written for this tile is brought to the new m_t).
+      // P is packed bf16 over the first 64 columns of this S tile: tokens
+      // 0..63 -> columns 0..31 (their scores are read before anything is
+      // written), then tokens 64..127 -> columns 32..63.
+      float m_t = m_run, l_t = 0.f;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         float v[64];
         tmem_ld64_sync(sbase + 64 * half, v);
-        scaled(v, half);
+        float hm = -INFINITY;
+        if (all_valid) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) mt = fmaxf(mt, v[j]);
+          for (int j = 0; j < 64; ++j) {
+            v[j] *= p.scale_log2;
+            hm = fmaxf(hm, v[j]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int t = 64 * half + j;
+            const bool ok = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
+            v[j] = ok ? v[j] * p.scale_log2 : -INFINITY;
+            hm = fmaxf(hm, v[j]);
+          }
+        }
+        const bool grow = hm > m_t + kRescaleThreshold || (m_t == -INFINITY && hm > -INFINITY);
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? hm : m_t;
+          if (half == 1) {
+            // bring this tile's first 32 columns of P to the new reference
+            const float f = (grow && m_t > -INFINITY) ? ex2_approx(m_t - m_new) : 1.f;
+            float qf[32];
+            tmem_ld32_sync(sbase, qf);
+            uint32_t q[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const uint32_t w = __float_as_uint(qf[j]);
+              q[j] = pack_bf16(bf16_lo(w) * f, bf16_hi(w) * f);
+            }
+            tmem_st32_sync(sbase, q);
+            l_t *= f;
+          }
+          m_t = m_new;
+        }
+        // m_t is -inf only while every score seen is -inf: those give P = 0
+        const float mref = m_t == -INFINITY ? 0.f : m_t;
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float e0 = ex2_approx(v[2 * j] - mref);
+          const float e1 = ex2_approx(v[2 * j + 1] - mref);
+          pk[j] = pack_bf16(e0, e1);
+          l_t += e0 + e1;  // the exact weights (P itself is rounded to bf16)
+        }
+        tmem_st32_sync(sbase + 32 * half, pk);
       }
-      const bool grow = mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY);
-      const float m_new = grow ? mt : m_run;
-      const bool need_rescale = grow && i > 0 && m_run > -INFINITY;
-      const float corr = need_rescale ? exp2f(m_run - m_new) : 1.f;
-      if (__any_sync(0xffffffffu, need_rescale)) {
+      // O and l hold earlier tiles against m_run: bring them to m_t
+      const bool moved = m_t != m_run && m_run > -INFINITY;
+      const float corr = moved ? ex2_approx(m_run - m_t) : 1.f;
+      if (__any_sync(0xffffffffu, moved)) {
         // O must hold PV(i-1) complete before it is rescaled
         if (!mbar_wait_warp(&s.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
@@ -360,26 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32_sync(lane_base + kOCol + 32 * cc, r);
         }
       }
-      l_run *= corr;
-      m_run = m_new;
-      // P = exp2(x - m) as packed bf16 over the first 64 columns of this S tile:
-      // tokens 0..63 -> columns 0..31 first (their scores are re-read before
-      // anything is written), then tokens 64..127 -> columns 32..63.
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float v[64];
-        tmem_ld64_sync(sbase + 64 * half, v);
-        scaled(v, half);
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float e0 = m_run == -INFINITY ? 0.f : exp2f(v[2 * j] - m_run);
-          const float e1 = m_run == -INFINITY ? 0.f : exp2f(v[2 * j + 1] - m_run);
-          pk[j] = pack_bf16(e0, e1);
-          l_run += bf16_lo(pk[j]) + bf16_hi(pk[j]);
-        }
-        tmem_st32_sync(sbase + 32 * half, pk);
-      }
+      l_run = l_run * corr + l_t;
+      m_run = m_t;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.p_full[buf]);

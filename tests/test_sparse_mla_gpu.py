@@ -23,14 +23,17 @@ def run_case(ctx, next_n, k, seed, holes=0.0):
     return mla, layout, idx, out, lse
 
 
-def compare(mla, layout, next_n, idx, out, lse, rows=None):
+def compare(mla, layout, next_n, idx, out, lse, rows=None, rel=0.0):
+    """rel adds rel * |ref| to the absolute bound, element by element: the
+    output is stored in bf16, whose rounding alone is up to 2^-9 * |ref|."""
     o_ref, l_ref = mla_oracle(mla, layout.block_table, next_n, idx, rows=rows)
     got = np_(out.float())
     gl = np_(lse)
     if rows is not None:
         got, gl = got[rows], gl[rows]
+    excess = np.abs(got - o_ref) - (MLA_ATOL + rel * np.abs(o_ref))
     err = np.abs(got - o_ref).max()
-    assert err <= MLA_ATOL, f"max |out - ref| = {err}"
+    assert excess.max() <= 0, f"max |out - ref| = {err}, worst excess {excess.max()}"
     fin = np.isfinite(l_ref)
     assert np.array_equal(np.isfinite(gl), fin)
     if fin.any():
@@ -67,3 +70,31 @@ def test_mla_index_order_does_not_matter_and_is_not_a_prefix():
     prefix = torch.arange(512, dtype=torch.int32, device="cuda")[None]
     out3, _ = gpu_mla(mla, layout.block_table, 1, 1, prefix, layout.num_pages)
     assert (out.float() - out3.float()).abs().max() > 0.05
+
+
+def test_mla_scores_growing_within_and_across_tiles():
+    """Scores that rise inside a 128-token tile (second half) and from tile to
+    tile, so the running softmax reference moves mid-tile (P already written
+    for the tile's first half is brought to the new reference) and between
+    tiles (O and l are rescaled).  Only the 64 rotary dimensions of the keys
+    are scaled: they enter the scores but not the values, so the outputs keep
+    their unit scale; but each output is then close to a single value row
+    (up to ~4.5), so the bound adds one bf16 ulp of the reference (2^-8 |ref|)
+    for the rounding of the stored output."""
+    ctx, k = [6000, 7000], 512
+    layout = W.make_layout(ctx, 7, device="cuda")
+    mla = W.make_mla_case(2, layout.num_pages, seed=7, device="cuda")
+    L = W.row_lengths(layout.ctx_len, 1).tolist()
+    idx = W.random_indices(L, k, seed=7, device="cuda")
+    kv = mla.kv.float()
+    bt = layout.block_table
+    for r in range(2):
+        toks = idx[r].long()
+        j = torch.arange(k, device="cuda")
+        factor = 1.0 + 19.0 * ((j % 128) >= 64).float() + 10.0 * (j // 128).float()
+        pages, slots = bt[r, toks // 64].long(), toks % 64
+        kv[pages, slots, 512:] *= factor[:, None]
+    mla.kv.copy_(kv.to(torch.bfloat16))
+    out, lse = gpu_mla(mla, layout.block_table, 2, 1, idx, layout.num_pages)
+    torch.cuda.synchronize()
+    compare(mla, layout, 1, idx, out, lse, rel=2.0 ** -8)
