@@ -239,72 +239,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait<0>();  // no copy of this thread is left in flight at exit
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
-    if (ntile > 0 && mbar_wait_warp(&s.q_full, 0, p.err, abort)) {
+    // One thread runs this role: the issue loop is on the critical path (an
+    // M=128 MMA holds the issuing thread for ~96-128 cycles), so it carries no
+    // warp votes or warp barriers.
+    if (lane == 0 && ntile > 0 && mbar_wait(&s.q_full, 0, p.err, abort)) {
       int g = 0;
       for (int i = 0; i <= ntile && !*abort; ++i) {
         bool bad = false;
         if (i < ntile) {
           const int buf = i & 1;
           // the S/P tile is reused after PV(i-2) has read P(i-2) from it
-          if (i >= 2 && !mbar_wait_warp(&s.pv_done[i & 1], ((i - 2) >> 1) & 1, p.err, abort)) break;
+          if (i >= 2 && !mbar_wait(&s.pv_done[i & 1], ((i - 2) >> 1) & 1, p.err, abort)) break;
           tc_fence_after();
           const uint32_t dS = s.tmem_base + kSCol + buf * kTile;
           for (int c = 0; c < kChunks; ++c, ++g) {
             const int slot = g % kRing;
-            if (!mbar_wait_warp(&s.full[slot], (g / kRing) & 1, p.err, abort)) { bad = true; break; }
+            if (!mbar_wait(&s.full[slot], (g / kRing) & 1, p.err, abort)) { bad = true; break; }
             fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core
             tc_fence_after();
-            if (lane == 0) {
-              const uint32_t a0 = smem_u32(s.q[c]);
-              const uint32_t b0 = smem_u32(s.ring[slot]);
+            const uint32_t a0 = smem_u32(s.q[c]);
+            const uint32_t b0 = smem_u32(s.ring[slot]);
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16(dS, sw128_desc(a0 + 32 * kk, 16, 1024),
-                        sw128_desc(b0 + 32 * kk, 16, 1024), kIdescS, (c | kk) != 0);
-              mma_commit(&s.empty[slot]);
-            }
-            __syncwarp();
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16(dS, sw128_desc(a0 + 32 * kk, 16, 1024), sw128_desc(b0 + 32 * kk, 16, 1024),
+                      kIdescS, (c | kk) != 0);
+            mma_commit(&s.empty[slot]);
           }
           if (bad) break;
-          if (lane == 0) mma_commit(&s.s_full[buf]);
-          __syncwarp();
+          mma_commit(&s.s_full[buf]);
         }
         if (i >= 1) {
           const int t = i - 1;  // PV of the previous tile
-          if (!mbar_wait_warp(&s.p_full[t & 1], (t >> 1) & 1, p.err, abort)) break;
+          if (!mbar_wait(&s.p_full[t & 1], (t >> 1) & 1, p.err, abort)) break;
           for (int j = 0; j < 4 && !bad; ++j) {
             const int gg = g + j;
-            bad = !mbar_wait_warp(&s.full[gg % kRing], (gg / kRing) & 1, p.err, abort);
+            bad = !mbar_wait(&s.full[gg % kRing], (gg / kRing) & 1, p.err, abort);
           }
           if (bad) break;
           fence_proxy_async_smem();
           tc_fence_after();
-          if (lane == 0) {
-            // value chunk j sits in slot (g + j) % kRing: one or two contiguous runs
-            const int first = g % kRing;
-            const int n1 = min(4, kRing - first);  // chunks in the first run
-            const uint32_t pa = s.tmem_base + kSCol + (t & 1) * kTile;
-            const uint32_t v0 = smem_u32(s.ring[first]);
-            const uint32_t v1 = smem_u32(s.ring[0]);
+          // value chunk j sits in slot (g + j) % kRing: one or two contiguous runs
+          const int first = g % kRing;
+          const int n1 = min(4, kRing - first);  // chunks in the first run
+          const uint32_t pa = s.tmem_base + kSCol + (t & 1) * kTile;
+          const uint32_t v0 = smem_u32(s.ring[first]);
+          const uint32_t v1 = smem_u32(s.ring[0]);
 #pragma unroll 1
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-              mma_f16_ts(s.tmem_base + kOCol, pa + 8 * kk,
-                         sw128_desc(v0 + 2048 * kk, kChunkBytes, 1024),
-                         make_idesc(1, 1, 128, 64 * n1, false, true), acc);
-              if (n1 < 4)
-                mma_f16_ts(s.tmem_base + kOCol + 64 * n1, pa + 8 * kk,
-                           sw128_desc(v1 + 2048 * kk, kChunkBytes, 1024),
-                           make_idesc(1, 1, 128, 64 * (4 - n1), false, true), acc);
-            }
-            for (int j = 0; j < 4; ++j) mma_commit(&s.empty[(g + j) % kRing]);
-            mma_commit(&s.pv_done[t & 1]);
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+            mma_f16_ts(s.tmem_base + kOCol, pa + 8 * kk,
+                       sw128_desc(v0 + 2048 * kk, kChunkBytes, 1024),
+                       make_idesc(1, 1, 128, 64 * n1, false, true), acc);
+            if (n1 < 4)
+              mma_f16_ts(s.tmem_base + kOCol + 64 * n1, pa + 8 * kk,
+                         sw128_desc(v1 + 2048 * kk, kChunkBytes, 1024),
+                         make_idesc(1, 1, 128, 64 * (4 - n1), false, true), acc);
           }
-          __syncwarp();
+          for (int j = 0; j < 4; ++j) mma_commit(&s.empty[(g + j) % kRing]);
+          mma_commit(&s.pv_done[t & 1]);
           g += 4;
         }
       }
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------ softmax / epilogue --
     const int quad = warp & 3;  // warps 8-11: TMEM lane quadrants 0-3
