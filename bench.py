@@ -13,7 +13,7 @@ same run and reported under "candidate_path".
 
 value = indexer keys scored (row, key pairs) per second of the whole step.
 All inputs are seeded synthetic data generated on the device; the key cache
-(553 MB) and the latent cache (4.8 GB) are larger than L2, so no flush is
+(553.6 MB) and the latent cache (4.8 GB) are larger than L2, so no flush is
 needed between steps.
 
 --impl reference times the fp64 CPU oracle (the reference arm) on bounded
@@ -34,6 +34,11 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# DRAM bytes (read + write) of one dsa_indexer_logits launch per cached token,
+# measured by ncu on this workload at 16 requests x 131072 tokens, next_n = 2
+# (`bench.py --requests 16 --no-candidate --no-cpu-baseline --steps 1
+# --warmup 1`, second indexer launch): 277.44 MB read + 14.16 MB written.
+INDEXER_DRAM_BYTES_PER_TOKEN = (277.44e6 + 14.16e6) / (16 * 131072)
 METRIC = "indexer keys scored/s + HBM GB/s at 128K decode; top-k rows/s; sparse-attn tok/s"
 WORKLOAD = ("128K MTP decode: 32 requests x 131072 ctx, next_n=2 (64 rows), FP8 indexer "
             "64x128 over 64-token shuffled pages, exact top-2048, sparse MLA 128 heads x "
@@ -354,6 +359,9 @@ def run_ours(args):
     # token read, 4 B logit per (row, key) written
     tokens = args.requests * 131072
     alg_bytes = tokens * 132 + keys_per_step * 4
+    # measured DRAM traffic of the indexer, scaled by the cached tokens (the
+    # traffic grows in proportion to them)
+    traffic = INDEXER_DRAM_BYTES_PER_TOKEN * tokens
     t_idx = per["indexer"] * 1e-3
     achieved = alg_bytes / t_idx / 1e9
     e2e_ms, h2d, d2h = e2e_decode(st, args.steps, args.warmup, stream)
@@ -393,7 +401,8 @@ def run_ours(args):
                        "(64 rows)", f"({2 * args.requests} rows)"),
                    "global_batch": 2 * args.requests * world, "seq_len": 131072,
                    "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (553.6 MB key cache, 4.8 GB latent cache); no flush"},
+                   "l2": f"inputs larger than L2 ({tokens * 132 / 1e6:.1f} MB key cache, "
+                         f"{tokens * 1152 / 1e9:.1f} GB latent cache); no flush"},
         "breakdown_ms": {k: round(v, 4) for k, v in per.items()},
         "indexer": {"keys_per_s": keys_per_step / t_idx, "hbm_gbs": achieved,
                     "unique_keys_per_s": tokens / t_idx},
@@ -404,7 +413,7 @@ def run_ours(args):
                        "tflops": R * 2 * 128 * TOPK * (576 + 512) / (per["sparse_mla"] * 1e-3) / 1e12},
         "candidate_path": cand,
         "roofline": {"kernel": "dsa_indexer_logits", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": peak_src,
                      "alg_bytes_per_launch": alg_bytes},
         "gpu_launches": args.steps * (len(kernels) + (1 if st["wsb"] > 0 else 0)) +
@@ -413,9 +422,6 @@ def run_ours(args):
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
     }
-    traffic = os.environ.get("DSA_INDEXER_TRAFFIC_BYTES")
-    if traffic:
-        line["roofline"]["traffic"] = float(traffic)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, dt, desc = cpu_baseline_sample(rows=args.cpu_rows)
         line["cpu_baseline"] = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle",
