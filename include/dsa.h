@@ -128,12 +128,12 @@ dsa_status dsa_indexer_logits(const uint8_t* q_fp8, const float* q_scale, const 
  * set equals the first k of a stable sort by score descending.  -0.0 == +0.0.
  * NaN logits are unsupported.
  *
- * Long rows (row_len >= 65536 for k >= 1024, >= 98304 for k < 1024) take the
- * cutoff path described for vLLM's persistent top-k: estimate a cutoff from a
- * sample, compact the survivors into shared memory in one pass over the row,
- * finish with an exact radix selection on them (redoing the row with the
- * full-row radix if the estimate missed).  Shorter rows take the full-row
- * radix select.  `force_path`: 0 = that rule, 1 = always full-row, 2 = always
+ * Long rows (row_len >= 8k, or longer than 40960) take the cutoff path
+ * described for vLLM's persistent top-k: estimate a cutoff from a sample,
+ * compact the survivors into shared memory in one pass over the row, finish
+ * with an exact selection on them (redoing the row with the full-row radix if
+ * the estimate missed).  Shorter rows take the full-row radix select over
+ * their keys staged in shared memory.  `force_path`: 0 = that rule, 1 = always full-row, 2 = always
  * cutoff (for tests; the selected set is the same).
  *
  *   logits     device [R, ld] f32; ld % 4 == 0, 16-byte aligned.
