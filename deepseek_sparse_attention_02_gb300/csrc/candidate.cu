@@ -265,11 +265,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     RowCursor cur;
     cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
     if (lane == 0) tma_prefetch_desc(&tm_q);
+    // The page of a tile column block takes two dependent loads (sparse
+    // index, then block table).  Lane l holds block 2*tile_begin + l of a
+    // chunk: its sparse index is loaded two chunks ahead and its page one chunk
+    // ahead, so no load sits on the copy issue path.
+    auto load_blk = [&](const RowCursor& c) -> int {
+      if (!c.valid() || lane >= 2 * kChunkTiles) return -1;
+      const int b = 2 * c.tile_begin() + lane;
+      return b < p.nb ? p.sparse_indices[static_cast<int64_t>(c.row) * p.nb + b] : -1;
+    };
+    auto load_page = [&](const RowCursor& c, int blk) -> int {
+      if (!c.valid() || lane >= 2 * kChunkTiles) return -1;
+      if (blk < 0 || blk >= p.bt_stride) return -2;
+      return p.bt[static_cast<int64_t>(c.row / p.next_n) * p.bt_stride + blk];
+    };
+    RowCursor ahead1 = cur, ahead2 = cur;
+    int pages_cur = load_page(cur, load_blk(cur));
+    if (ahead1.valid()) ahead1.next();
+    int blk1 = load_blk(ahead1);
+    ahead2 = ahead1;
+    if (ahead2.valid()) ahead2.next();
+    int blk2 = load_blk(ahead2);
+    int pages1 = load_page(ahead1, blk1);
     int lt = 0;
     bool new_group = true;
     while (cur.valid() && !*abort) {
       const int r = cur.row;
-      const int req = r / p.next_n;
       if (new_group) {
         const int slot = cur.gcount & 1;
         const int use = cur.gcount >> 1;
@@ -284,21 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int endr = min(p.end[r], p.nb * 64);
+      const int tb = cur.tile_begin();
       bool bad = false;
-      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+      for (int t = tb; t < cur.tile_end(); ++t, ++lt) {
         const int st = lt % kStages;
         const int use = lt / kStages;
         if (use > 0 && !mbar_wait_warp(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
+        int pid[2];
+        pid[0] = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb));
+        pid[1] = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb) + 1);
         if (lane == 0) {
           const bool two = (2 * t + 1) * 64 < endr;
           mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kPackedPage + kSfPage));
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (h == 1 && !two) break;
-            const int blk = p.sparse_indices[static_cast<int64_t>(r) * p.nb + 2 * t + h];
-            int page = -1;
-            if (blk >= 0 && blk < p.bt_stride)
-              page = p.bt[static_cast<int64_t>(req) * p.bt_stride + blk];
+            int page = pid[h];
             if (page < 0 || page >= p.num_pages) {
               raise_error(p.err, kErrBadPage);
               page = 0;
@@ -315,6 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (bad) break;
       new_group = cur.next();
+      pages_cur = pages1;
+      ahead1 = ahead2;
+      blk1 = blk2;
+      if (ahead2.valid()) ahead2.next();
+      blk2 = load_blk(ahead2);
+      pages1 = load_page(ahead1, blk1);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer --
