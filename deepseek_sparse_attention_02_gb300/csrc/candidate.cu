@@ -26,8 +26,13 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kStages = 6;
+// warp 0 producer, warp 1 MMA issuer, warps 2-5 converters, warps 6-13 two
+// epilogue warpgroups
+constexpr int kConvWarp = 2;
+constexpr int kFirstEpiWarp = 6;
+constexpr int kThreads = 32 * (kFirstEpiWarp + 8);
+constexpr int kStages = 8;  // raw (packed + scale) stages
+constexpr int kA = 4;       // converted e4m3 tiles; even, so a slot has one epilogue warpgroup
 constexpr int kTileCols = 128;
 constexpr int kChunkTiles = 4;
 constexpr uint32_t kPackedPage = 64 * 64;  // 4096
@@ -197,14 +202,15 @@ struct RowCursor {
 };
 
 struct CSmem {
-  uint8_t a[2][128 * 128];           // converted e4m3 key tiles, K-major SW128
+  uint8_t a[kA][128 * 128];          // converted e4m3 key tiles, K-major SW128
   uint8_t q[2][64 * 128];            // q of the row, K-major SW128
   uint8_t raw[kStages][2 * kPackedPage];
   uint8_t sf[kStages][2 * kSfPage];
   float wq[2][64];
   uint64_t full[kStages], empty[kStages];
   uint64_t qfull[2], qempty[2];
-  uint64_t afull[2], tfull[2], tempty[2];
+  uint32_t ascale[kA][128];          // UE8M0 scale words of each converted tile's rows
+  uint64_t afull[kA], aempty[kA], tfull[2], tempty[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -239,12 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 4);
+      mbar_init(&s.empty[i], 4);  // the 4 converter warps
+    }
+    for (int i = 0; i < kA; ++i) {
+      mbar_init(&s.afull[i], 4);      // the 4 converter warps
+      mbar_init(&s.aempty[i], 1 + 4); // MMA commit + the 4 epilogue warps that read the scales
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.qfull[i], 32);
       mbar_init(&s.qempty[i], 1 + 8);
-      mbar_init(&s.afull[i], 4);  // one arrival per converting warp
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], 4);
     }
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ahead2.valid()) ahead2.next();
     int blk2 = load_blk(ahead2);
     int pages1 = load_page(ahead1, blk1);
-    int lt = 0;
+    int lt = 0, endr = 0;
     bool new_group = true;
     while (cur.valid() && !*abort) {
       const int r = cur.row;
@@ -304,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&s.qfull[slot]);
         }
       }
-      const int endr = min(p.end[r], p.nb * 64);
+      if (new_group) endr = min(p.end[r], p.nb * 64);
       const int tb = cur.tile_begin();
       bool bad = false;
       for (int t = tb; t < cur.tile_end(); ++t, ++lt) {
@@ -345,41 +354,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       pages1 = load_page(ahead1, blk1);
     }
   } else if (warp == 1) {
-    // ----------------------------------------------------------- MMA issuer --
-    RowCursor cur;
-    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
-    int lt = 0;
-    bool new_group = true;
-    while (cur.valid() && !*abort) {
-      const int slot = cur.gcount & 1;
-      if (new_group && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
-      bool bad = false;
-      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
-        const int buf = lt & 1;
-        const int ub = lt >> 1;
-        if (!mbar_wait_warp(&s.afull[buf], ub & 1, p.err, abort)) { bad = true; break; }
-        if (ub > 0 && !mbar_wait_warp(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(s.a[buf]);
-          const uint32_t b0 = smem_u32(s.q[slot]);
+    // ---------------------------------------------------------- MMA issuer --
+    // One thread: the per-tile loop carries no warp votes or warp barriers.
+    if (lane == 0) {
+      RowCursor cur;
+      cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
+      int lt = 0;
+      bool new_group = true;
+      while (cur.valid() && !*abort) {
+        const int slot = cur.gcount & 1;
+        if (new_group && !mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
+        bool bad = false;
+        const uint32_t b0 = smem_u32(s.q[slot]);
+        for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+          const int ac = lt % kA;
+          const int buf = lt & 1;
+          const int ub = lt >> 1;
+          if (!mbar_wait(&s.afull[ac], (lt / kA) & 1, p.err, abort)) { bad = true; break; }
+          if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(s.a[ac]);
           const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * 256);
 #pragma unroll
           for (int g = 0; g < 4; ++g)
             mma_f8f6f4(d + 64 * g, sw128_desc(a0 + 32 * g, 16, 1024),
                        sw128_desc(b0 + 32 * g, 16, 1024), kIdesc, 0);
+          mma_commit(&s.aempty[ac]);
           mma_commit(&s.tfull[buf]);
         }
+        if (bad) break;
+        new_group = cur.next();
+        if (new_group) mma_commit(&s.qempty[slot]);
+      }
+    }
+    __syncwarp();
+  } else if (warp < kFirstEpiWarp) {
+    // ---------------------------------------------------------- converters --
+    // A warp expands 8 token rows per step: lane l takes 16 packed bytes
+    // (piece l % 4 of row l / 4; a warp's loads are 512 contiguous bytes) and
+    // writes the 32 e4m3 bytes they expand to (two 16-byte chunks of the
+    // 128B-swizzled row; balanced over the banks).  Each warp also passes on
+    // the UE8M0 scale words of its 32 rows with the tile.
+    const int cw = warp - kConvWarp;  // rows [32 cw, 32 cw + 32) of every tile
+    const int piece = lane & 3;
+    RowCursor cur;
+    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
+    int lt = 0;
+    while (cur.valid() && !*abort) {
+      bool bad = false;
+      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        const int st = lt % kStages;
+        const int ac = lt % kA;
+        if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
+        if (lt >= kA && !mbar_wait_warp(&s.aempty[ac], ((lt / kA) - 1) & 1, p.err, abort)) { bad = true; break; }
+        uint8_t* dst = s.a[ac];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int tr = 32 * cw + 8 * it + (lane >> 2);
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              s.raw[st] + (tr >> 6) * kPackedPage + (tr & 63) * 64 + 16 * piece);
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            o[2 * u] = e2m1x4_to_e4m3(in[u]);
+            o[2 * u + 1] = e2m1x4_to_e4m3(in[u] >> 16);
+          }
+          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * piece)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * piece + 1)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        {
+          const int tr = 32 * cw + lane;
+          s.ascale[ac][tr] =
+              *reinterpret_cast<const uint32_t*>(s.sf[st] + (tr >> 6) * kSfPage + (tr & 63) * 4);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes of the tile -> tensor core
         __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s.afull[ac]);
+          mbar_arrive(&s.empty[st]);
+        }
       }
       if (bad) break;
-      new_group = cur.next();
-      if (new_group && lane == 0) mma_commit(&s.qempty[slot]);
-      __syncwarp();
+      cur.next();
     }
   } else {
-    // -------------------------------------- convert + epilogue warpgroups --
-    const int wg = (warp - 2) >> 2;
+    // ------------------------------------------------------------ epilogue --
+    const int wg = (warp - kFirstEpiWarp) >> 2;  // drains the tiles (and accumulator) == wg (mod 2)
     const int quad = warp & 3;
     const int tr = quad * 32 + lane;  // token row of the tile == TMEM lane
     RowCursor cur;
@@ -392,45 +455,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool waited_q = false, bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
         if ((lt & 1) != wg) continue;
-        const int st = lt % kStages;
-        if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
-        // expand this thread's token row: 64 packed bytes -> 128 e4m3 bytes
-        const uint8_t* src = s.raw[st] + (tr >> 6) * kPackedPage + (tr & 63) * 64;
-        uint8_t* dst = s.a[wg];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * j);
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            o[2 * u] = e2m1x4_to_e4m3(in[u]);
-            o[2 * u + 1] = e2m1x4_to_e4m3(in[u] >> 16);
-          }
-          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * j)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * j + 1)) =
-              make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        const uint32_t sfw =
-            *reinterpret_cast<const uint32_t*>(s.sf[st] + (tr >> 6) * kSfPage + (tr & 63) * 4);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&s.afull[wg]);
-          mbar_arrive(&s.empty[st]);
-        }
-        float sc[4];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) sc[g] = ue8m0_to_float((sfw >> (8 * g)) & 0xffu);
+        const int ac = lt % kA;
         if (!waited_q) {
           if (!mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
           waited_q = true;
         }
         if (!mbar_wait_warp(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
+        const uint32_t sfw = s.ascale[ac][tr];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.aempty[ac]);
+        float sc[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) sc[g] = ue8m0_to_float((sfw >> (8 * g)) & 0xffu);
         const uint32_t taddr = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(wg * 256);
-        float acc = 0.f;
+        float acc[2] = {0.f, 0.f};
 #pragma unroll
         for (int hc = 0; hc < 4; ++hc) {
           float d0[16], d1[16], d2[16], d3[16];
@@ -442,14 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
             const float x = fmaf(sc[3], d3[h], fmaf(sc[2], d2[h], fmaf(sc[1], d1[h], sc[0] * d0[h])));
-            acc = fmaf(wh[h], fmaxf(x, 0.f), acc);
+            acc[h & 1] = fmaf(wh[h], fmaxf(x, 0.f), acc[h & 1]);
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.tempty[wg]);
         const int col = t * kTileCols + tr;
-        if (col < endr) p.logits[static_cast<int64_t>(r) * p.ld + col] = acc;
+        if (col < endr) p.logits[static_cast<int64_t>(r) * p.ld + col] = acc[0] + acc[1];
       }
       if (bad) break;
       // A warp may walk through a group without processing any of its tiles (they
