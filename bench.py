@@ -309,6 +309,11 @@ def dist_setup():
     return world, rank, local, pg
 
 
+def aggregate_value(world: int, units_per_rank: float, ms_max: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's step."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def reduce_max(pg, value: float, device):
     if pg is None:
         return value
@@ -353,7 +358,7 @@ def run_ours(args):
     ms_step_max = reduce_max(pg, ms_step, device)
 
     keys_per_step = float(st["L"].sum().item())
-    value = world * keys_per_step / (ms_step_max * 1e-3)
+    value = aggregate_value(world, keys_per_step, ms_step_max)
     hbm, bf16_tf, peak_src = peaks()
     # dominant kernel: the indexer (HBM-bound): 128 B key + 4 B scale per cached
     # token read, 4 B logit per (row, key) written
