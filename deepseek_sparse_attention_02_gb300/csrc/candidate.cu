@@ -288,6 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (blk < 0 || blk >= p.bt_stride) return -2;
       return p.bt[static_cast<int64_t>(c.row / p.next_n) * p.bt_stride + blk];
     };
+    // keys are read once per layer: their lines go first out of L2, which
+    // leaves the logits written here in L2 for the top-k that reads them next
+    const uint64_t evict_first = l2_policy_evict_first();
     RowCursor ahead1 = cur, ahead2 = cur;
     int pages_cur = load_page(cur, load_blk(cur));
     if (ahead1.valid()) ahead1.next();
@@ -334,12 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               raise_error(p.err, kErrBadPage);
               page = 0;
             }
-            bulk_load(s.raw[st] + h * kPackedPage,
-                      p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride, kPackedPage,
-                      &s.full[st]);
-            bulk_load(s.sf[st] + h * kSfPage,
-                      p.k_sf + static_cast<int64_t>(page) * p.sf_page_stride, kSfPage,
-                      &s.full[st]);
+            bulk_load_hint(s.raw[st] + h * kPackedPage,
+                           p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride, kPackedPage,
+                           &s.full[st], evict_first);
+            bulk_load_hint(s.sf[st] + h * kSfPage,
+                           p.k_sf + static_cast<int64_t>(page) * p.sf_page_stride, kSfPage,
+                           &s.full[st], evict_first);
           }
         }
         __syncwarp();
