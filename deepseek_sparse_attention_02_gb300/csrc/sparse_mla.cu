@@ -17,11 +17,12 @@
 //              selections, running max with lazy rescaling of O (only when the
 //              max grows by more than 2^8), P = exp2(S*scale*log2e - m) packed as
 //              bf16 into the TMEM columns of the S tile it came from;
-//   warp 12    tcgen05 issuer, in the order S(0), S(1), PV(0), S(2), PV(1), ...:
-//              S = Q K^T (kind::f16, M = 128 heads, N = 128 tokens, K = 576)
-//              into one of two TMEM tiles; O[128 x 256] += P V_half with P read
-//              from TMEM and V read MN-major from the ring (N = 256 when the
-//              four value chunks are contiguous in the ring, else two MMAs).
+//   warp 12    tcgen05 issuer of S = Q K^T (kind::f16, M = 128 heads, N = 128
+//              tokens, K = 576) into one of two TMEM tiles;
+//   warp 13    tcgen05 issuer of O[128 x 256] += P V_half with P read from TMEM
+//              and V read MN-major from the ring (N = 256 when the four value
+//              chunks are contiguous in the ring, else two MMAs).  The ring
+//              holds, in order, S(0), S(1), PV(0), S(2), PV(1), ...
 // Many gathering warps matter: scattered 128-byte latent lines reach ~4-5 TB/s
 // this way, about twice the rate of TMA tile::gather4 for the same lines.
 // The 512 value columns are split over two CTAs because O for 128 heads x 512
@@ -40,8 +41,9 @@ namespace dsa {
 namespace {
 
 constexpr int kGatherWarps = 8;
-constexpr int kThreads = 32 * (kGatherWarps + 4 + 1);  // gather, softmax, MMA
+constexpr int kThreads = 32 * (kGatherWarps + 4 + 2);  // gather, softmax, S MMA, PV MMA
 constexpr int kMmaWarp = kGatherWarps + 4;
+constexpr int kPvWarp = kMmaWarp + 1;
 constexpr int kRing = 5;
 constexpr int kTile = 128;
 constexpr int kChunks = 9;  // 576 / 64
@@ -75,7 +77,10 @@ struct MSmem {
   uint8_t q[kChunks][kHeads * 128];  // 9 x 16 KB, K-major SW128, rows = heads
   uint8_t ring[kRing][kChunkBytes];  // [128 tokens x 64 elems] bf16 SW128
   uint64_t q_full;
-  uint64_t full[kRing], empty[kRing];
+  // a slot's use is signalled on full[] (an S chunk) or fullv[] (a value
+  // chunk): each barrier has one consumer thread, which waits every phase
+  // in order, so a parity wait cannot pass on an older phase
+  uint64_t full[kRing], fullv[kRing], empty[kRing];
   uint64_t s_full[2];
   uint64_t p_full[2], pv_done[2];  // per S/P tile: tile t uses index t & 1
   uint32_t tmem_base;
@@ -83,9 +88,8 @@ struct MSmem {
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-  return lo | (hi << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -126,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.q_full, 1);
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&s.full[i], 32 * kGatherWarps);  // one cp.async completion per gather thread
+      mbar_init(&s.fullv[i], 32 * kGatherWarps);
       mbar_init(&s.empty[i], 1);
     }
     mbar_init(&s.s_full[0], 1);
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int g = 0;  // ring sequence number
     bool bad = false;
-    auto issue = [&](int c, const int (&r)[4]) -> bool {
+    auto issue = [&](int c, const int (&r)[4], bool value) -> bool {
       const int slot = g % kRing;
       if (g >= kRing && !mbar_wait_warp(&s.empty[slot], ((g / kRing) - 1) & 1, p.err, abort))
         return false;
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           cp_async_16_zero(d, p.kv);
       }
-      cp_async_mbar_arrive_noinc(&s.full[slot]);
+      cp_async_mbar_arrive_noinc(value ? &s.fullv[slot] : &s.full[slot]);
       ++g;
       return true;
     };
@@ -224,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_toks(i + 2, tk_after);
       }
       if (i < ntile)
-        for (int c = 0; c < kChunks && !bad; ++c) bad = !issue(c, rows_cur);
+        for (int c = 0; c < kChunks && !bad; ++c) bad = !issue(c, rows_cur, false);
       if (i >= 1)
-        for (int j = 0; j < 4 && !bad; ++j) bad = !issue(4 * vh + j, rows_prev);
+        for (int j = 0; j < 4 && !bad; ++j) bad = !issue(4 * vh + j, rows_prev, true);
       int rows_next[4] = {-1, -1, -1, -1};
       if (i + 1 < ntile) make_rows(tk_next, pg_next, rows_next);
 #pragma unroll
@@ -238,15 +243,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cp_async_wait<0>();  // no copy of this thread is left in flight at exit
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer --
-    // One thread runs this role: the issue loop is on the critical path (an
-    // M=128 MMA holds the issuing thread for ~96-128 cycles), so it carries no
-    // warp votes or warp barriers.
+    // -------------------------------------------------------- S MMA issuer --
+    // One thread runs each MMA role: an M=128 MMA holds the issuing thread for
+    // ~96-128 cycles, longer than the tensor core needs for it, so S (this
+    // warp) and P V (the next warp) are issued by two threads.  Their MMAs
+    // touch disjoint TMEM (S(i+1) its tile, PV(i) P(i) and O), and each
+    // thread's commits track only its own MMAs.  Ring order: S(0), then per
+    // tile i >= 1 S(i) followed by PV(i-1), and PV(ntile-1) last; S(i) starts
+    // at ring sequence number 13 i - 4 (i >= 1).
     if (lane == 0 && ntile > 0 && mbar_wait(&s.q_full, 0, p.err, abort)) {
-      int g = 0;
-      for (int i = 0; i <= ntile && !*abort; ++i) {
+      uint32_t phase = 0;  // bit j: parity of the next phase of full[j]
+      for (int i = 0; i < ntile && !*abort; ++i) {
         bool bad = false;
-        if (i < ntile) {
+        int g = i == 0 ? 0 : (kChunks + 4) * i - 4;
+        {
           const int buf = i & 1;
           // the S/P tile is reused after PV(i-2) has read P(i-2) from it
           if (i >= 2 && !mbar_wait(&s.pv_done[i & 1], ((i - 2) >> 1) & 1, p.err, abort)) break;
@@ -254,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dS = s.tmem_base + kSCol + buf * kTile;
           for (int c = 0; c < kChunks; ++c, ++g) {
             const int slot = g % kRing;
-            if (!mbar_wait(&s.full[slot], (g / kRing) & 1, p.err, abort)) { bad = true; break; }
+            if (!mbar_wait(&s.full[slot], (phase >> slot) & 1, p.err, abort)) { bad = true; break; }
+            phase ^= 1u << slot;
             fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core
             tc_fence_after();
             const uint32_t a0 = smem_u32(s.q[c]);
@@ -268,12 +279,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (bad) break;
           mma_commit(&s.s_full[buf]);
         }
-        if (i >= 1) {
-          const int t = i - 1;  // PV of the previous tile
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------- PV MMA issuer --
+    // PV(t) reads ring sequence numbers 13 t + 18 .. (after S(t+1)), or
+    // 13 t + 9 .. for the last tile.
+    if (lane == 0 && ntile > 0) {
+      uint32_t phase = 0;  // bit j: parity of the next phase of fullv[j]
+      for (int t = 0; t < ntile && !*abort; ++t) {
+        bool bad = false;
+        const int g = t + 1 < ntile ? (kChunks + 4) * t + 18 : (kChunks + 4) * t + kChunks;
+        {
           if (!mbar_wait(&s.p_full[t & 1], (t >> 1) & 1, p.err, abort)) break;
           for (int j = 0; j < 4 && !bad; ++j) {
             const int gg = g + j;
-            bad = !mbar_wait(&s.full[gg % kRing], (gg / kRing) & 1, p.err, abort);
+            const int slot = gg % kRing;
+            bad = !mbar_wait(&s.fullv[slot], (phase >> slot) & 1, p.err, abort);
+            phase ^= 1u << slot;
           }
           if (bad) break;
           fence_proxy_async_smem();
@@ -297,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int j = 0; j < 4; ++j) mma_commit(&s.empty[(g + j) % kRing]);
           mma_commit(&s.pv_done[t & 1]);
-          g += 4;
         }
       }
     }
@@ -342,12 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int half = 0; half < 2; ++half) {
         float v[64];
         tmem_ld64_sync(sbase + 64 * half, v);
-        float hm = -INFINITY;
+        float h4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (all_valid) {
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             v[j] *= p.scale_log2;
-            hm = fmaxf(hm, v[j]);
+            h4[j & 3] = fmaxf(h4[j & 3], v[j]);
           }
         } else {
 #pragma unroll
@@ -355,9 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = 64 * half + j;
             const bool ok = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
             v[j] = ok ? v[j] * p.scale_log2 : -INFINITY;
-            hm = fmaxf(hm, v[j]);
+            h4[j & 3] = fmaxf(h4[j & 3], v[j]);
           }
         }
+        const float hm = fmaxf(fmaxf(h4[0], h4[1]), fmaxf(h4[2], h4[3]));
         const bool grow = hm > m_t + kRescaleThreshold || (m_t == -INFINITY && hm > -INFINITY);
         if (__any_sync(0xffffffffu, grow)) {
           const float m_new = grow ? hm : m_t;
@@ -380,13 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // m_t is -inf only while every score seen is -inf: those give P = 0
         const float mref = m_t == -INFINITY ? 0.f : m_t;
         uint32_t pk[32];
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float e0 = ex2_approx(v[2 * j] - mref);
           const float e1 = ex2_approx(v[2 * j + 1] - mref);
           pk[j] = pack_bf16(e0, e1);
-          l_t += e0 + e1;  // the exact weights (P itself is rounded to bf16)
+          l4[j & 3] += e0 + e1;  // the exact weights (P itself is rounded to bf16)
         }
+        l_t += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_st32_sync(sbase + 32 * half, pk);
       }
       // O and l hold earlier tiles against m_run: bring them to m_t
