@@ -2,9 +2,12 @@
 // V3.2-Exp support", section "1. Architecture").
 //
 // One CTA of 1024 threads owns a row (persistent over rows, one CTA per SM).
-// Every pass synchronises with __syncthreads only: measured on GB300, one such
-// CTA streams a 512 KB row in ~6 us, while the cross-CTA histogram merges of a
-// cluster-per-row design cost ~2-3 us per radix pass.
+// Every radix pass synchronises with __syncthreads only: measured on GB300,
+// the cross-CTA histogram merges of a cluster-per-row design cost ~2-3 us per
+// pass.  When the rows are few (at most half the SM count) a second CTA per
+// row (a cluster of two) takes half of the one streaming pass below: that pass
+// is bound by the loads one CTA keeps in flight (~26 B/clk from L2), not by
+// its instructions, so two SMs halve it; the select itself stays on one CTA.
 //
 // Selection is a most-significant-digit radix select (11-bit digits) on the
 // 64-bit key  (order-preserving u32 of the f32 score) << 32 | ~column,  which
@@ -23,8 +26,12 @@
 //    estimate missed (fewer than k survivors, or more than fit) the row is
 //    redone by the radix select reading the row from global memory, so the
 //    result is always exact.
+#include <cooperative_groups.h>
+
 #include "internal.h"
 #include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 namespace {
@@ -58,8 +65,8 @@ struct TkSmem {
   uint32_t sample[kSample];
   uint32_t hist[2048];    // radix histogram (kBins)
   uint32_t wscan[kWarps]; // per-warp scan totals
-  uint32_t wsum[kWarps];  // per-warp survivor counts
-  uint32_t wmax[kWarps];  // per-warp largest survivor key
+  uint32_t wsum[2 * kWarps];  // per-region survivor counts (a region per warp of the row's CTAs)
+  uint32_t wmax[2 * kWarps];  // per-region largest survivor key
   uint32_t counter;       // output cursor
   uint32_t bin, above, binc;
   uint32_t ncand;         // candidates gathered from the boundary bin
@@ -179,19 +186,25 @@ struct SrcStaged {  // the row's keys staged in shared memory, in column order
   }
 };
 
-struct SrcPairs {  // survivors: warp w's are keys/cols [w*kWarpCap, w*kWarpCap + cnt[w])
+// Survivors: warp w's region is keys/cols [w*kWarpCap, (w+1)*kWarpCap); the
+// row's first CTA filled cnt[w] slots from the bottom, a second CTA (if any)
+// cnt[kWarps + w] slots from the top (cnt[w] + cnt[kWarps + w] <= kWarpCap,
+// else the row overflowed and is not visited this way).
+struct SrcPairs {
   const uint32_t* keys;
   const uint32_t* cols;
   const uint32_t* cnt;
   template <class F>
   __device__ void visit(F&& f) const {
-    const int lane = threadIdx.x & 31;
-    const int w0 = (threadIdx.x >> 5) * kWarpCap;  // each warp walks its own region
-    const int n = static_cast<int>(min(cnt[threadIdx.x >> 5], static_cast<uint32_t>(kWarpCap)));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int w0 = warp * kWarpCap;  // each warp walks its own region
+    const int n0 = static_cast<int>(cnt[warp]);
+    const int n = n0 + static_cast<int>(cnt[kWarps + warp]);
     const int lim = (n + 31) & ~31;
     for (int i = lane; i < lim; i += 32) {
       const bool ok = i < n;
-      f(ok ? keys[w0 + i] : 0u, ok ? ~cols[w0 + i] : 0u, ok);
+      const int j = w0 + (i < n0 ? i : kWarpCap - 1 - (i - n0));
+      f(ok ? keys[j] : 0u, ok ? ~cols[j] : 0u, ok);
     }
   }
 };
@@ -378,17 +391,21 @@ __device__ uint32_t local_tau(const uint32_t* sample, int n, uint32_t q, uint32_
   return tau;
 }
 
-// One streaming pass over the row: every element with key >= tau goes to its
-// warp's region of (keys, cols) (warp w owns [w*kWarpCap, (w+1)*kWarpCap) and
-// keeps its running count in a register, so the pass takes no atomics).
-// s.wsum[w] receives the warp's count (it may exceed kWarpCap: the caller
-// then treats the row as overflowed) and s.wmax[w] its largest kept key (0 if
-// none).  For tau above key(+0.0), key_of(x) >= tau is exactly the signed
-// compare of x's bits with tau's float bits (negative values, -0.0 and -NaN
-// fall below, +NaN above, as in key_of): one instruction per element.
-template <bool kPositiveTau>
-__device__ void compact(const SrcGlobal& g, uint32_t tau, uint32_t* keys, uint32_t* cols,
-                        TkSmem& s) {
+// One streaming pass over the columns [col0, col0 + g.n) of the row (g.row
+// points at column col0): every element with key >= tau goes to its warp's
+// region of (keys, cols), [w*kWarpCap, (w+1)*kWarpCap), filled from the bottom
+// (top = false) or from the top; the warp keeps its running count in a
+// register, so the pass takes no atomics.  wsum[w] receives the warp's count
+// (the caller treats the row as overflowed if the counts of a region exceed
+// kWarpCap; slots past kWarpCap are not written) and wmax[w] its largest kept
+// key (0 if none).  The destinations may be another CTA's shared memory
+// (generic addresses in the cluster window).  For tau above key(+0.0),
+// key_of(x) >= tau is exactly the signed compare of x's bits with tau's float
+// bits (negative values, -0.0 and -NaN fall below, +NaN above, as in key_of):
+// one instruction per element.
+template <bool kPositiveTau, bool kTop>
+__device__ void compact(const SrcGlobal& g, uint32_t col0, uint32_t tau, uint32_t* keys,
+                        uint32_t* cols, uint32_t* wsum, uint32_t* wmax) {
   constexpr int kB = 4;  // float4 loads per batch
   const int n = g.n;
   const int n4 = (n + 3) >> 2;
@@ -440,8 +457,9 @@ __device__ void compact(const SrcGlobal& g, uint32_t tau, uint32_t* keys, uint32
       const uint32_t key = key_of(ldg_nc(g.row + e));
       kmax = max(kmax, key);
       if (pos < static_cast<uint32_t>(kWarpCap)) {
-        wkeys[pos] = key;
-        wcols[pos] = static_cast<uint32_t>(e);
+        const uint32_t j = kTop ? kWarpCap - 1 - pos : pos;
+        wkeys[j] = key;
+        wcols[j] = col0 + static_cast<uint32_t>(e);
       }
       ++pos;
     }
@@ -449,8 +467,8 @@ __device__ void compact(const SrcGlobal& g, uint32_t tau, uint32_t* keys, uint32
   }
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) {
-    s.wsum[warp] = wcount;
-    s.wmax[warp] = kmax;
+    wsum[warp] = wcount;
+    wmax[warp] = kmax;
   }
 }
 
@@ -483,13 +501,27 @@ __device__ void emit(const Src& src, uint64_t thr, const TkParams& p, int row, T
   });
 }
 
+// kCsize = CTAs per row: 1, or 2 (a cluster).  The two are separate kernels:
+// measured on GB300, merely containing cluster instructions cost the one-CTA
+// kernel ~2 us per launch.
+template <int kCsize>
 __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
   extern __shared__ uint8_t smem_raw[];
   TkSmem& s =
       *reinterpret_cast<TkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
   const int tid = threadIdx.x;
+  // With two CTAs per row (a cluster of two, used when the rows are few) both
+  // derive the same cutoff from the row's sample, each compacts half of the
+  // row, rank 1 into regions kWarps..2 kWarps-1 of rank 0's shared memory, and
+  // rank 0 runs the exact select and the output.
+  constexpr int csize = kCsize;
+  int rank = 0;
+  if constexpr (kCsize > 1) rank = static_cast<int>(cg::this_cluster().block_rank());
+  TkSmem* s0p = &s;
+  if constexpr (kCsize > 1) s0p = cg::this_cluster().map_shared_rank(&s, 0);
+  TkSmem& s0 = *s0p;
 
-  for (int row = blockIdx.x; row < p.R; row += gridDim.x) {
+  for (int row = blockIdx.x / csize; row < p.R; row += gridDim.x / csize) {
     const float* rowp = p.logits + static_cast<int64_t>(row) * p.ld;
     int L = p.row_len[row];
     if (L < 0) L = 0;
@@ -501,7 +533,8 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
 
     if (L <= p.k) {
       // every column is selected; the tail is -1
-      for (int c = tid; c < p.k; c += kT) out[c] = c < L ? map_col(p, row, c) : -1;
+      if (rank == 0)
+        for (int c = tid; c < p.k; c += kT) out[c] = c < L ? map_col(p, row, c) : -1;
       continue;
     }
 
@@ -539,32 +572,51 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
       const uint32_t q = static_cast<uint32_t>(want < ns ? want : ns);
       // the survivor area is free until the compaction: it holds the bins
       const uint32_t tau = local_tau(s.sample, ns, q > 0 ? q : 1u, s.data, s);
-      // 2. one streaming pass: compact the survivors (key >= tau)
-      uint32_t* skeys = s.data;
-      uint32_t* scols = s.data + kWarps * kWarpCap;
-      const SrcGlobal g{rowp, L};
-      if (tau > 0x80000000u) compact<true>(g, tau, skeys, scols, s);
-      else compact<false>(g, tau, skeys, scols, s);
-      __syncthreads();
-      uint32_t total = 0, cmax = 0;
-      bool over = false;
-#pragma unroll 8
-      for (int w = 0; w < kWarps; ++w) {
-        total += s.wsum[w];
-        over |= s.wsum[w] > static_cast<uint32_t>(kWarpCap);
-        cmax = max(cmax, s.wmax[w]);
+      // 2. one streaming pass: compact the survivors (key >= tau); with two
+      // CTAs, columns [0, h) and [h, L), h a multiple of 4 (16-byte loads)
+      const int h = csize > 1 ? ((L + 7) >> 3) << 2 : L;
+      const int c0 = rank == 0 ? 0 : h;
+      const int c1 = rank == 0 ? h : L;
+      const SrcGlobal g{rowp + c0, c1 - c0};
+      uint32_t* const kw = s.data;
+      uint32_t* const cw = s.data + kWarps * kWarpCap;
+      if (rank == 0) {  // this CTA's shared memory, filled from the bottom
+        if (tau > 0x80000000u) compact<true, false>(g, c0, tau, kw, cw, s.wsum, s.wmax);
+        else compact<false, false>(g, c0, tau, kw, cw, s.wsum, s.wmax);
+        if (csize == 1 && tid < kWarps) s.wsum[kWarps + tid] = 0;  // no top fill
+      } else if constexpr (kCsize > 1) {  // rank 0's, through the cluster window, from the top
+        uint32_t* const kr = s0.data;
+        uint32_t* const cr = s0.data + kWarps * kWarpCap;
+        if (tau > 0x80000000u)
+          compact<true, true>(g, c0, tau, kr, cr, s0.wsum + kWarps, s0.wmax + kWarps);
+        else
+          compact<false, true>(g, c0, tau, kr, cr, s0.wsum + kWarps, s0.wmax + kWarps);
       }
-      if (!over && total >= static_cast<uint32_t>(p.k)) {
-        const SrcPairs sp{skeys, scols, s.wsum};
-        static_assert(kBins % kT == 0 && kBins <= 2048, "hist holds kBins bins");
-        const uint64_t thr = survivor_select(sp, p.k, tau, cmax, s);
-        emit(sp, thr, p, row, s);
-        done = true;
-      } else if (tid == 0) {
-        raise_error(p.err, kErrCapacity);
+      if constexpr (kCsize > 1) cg::this_cluster().sync();  // rank 1's survivors are in place
+      else __syncthreads();
+      if (rank == 0) {
+        uint32_t total = 0, cmax = 0;
+        bool over = false;
+#pragma unroll 8
+        for (int w = 0; w < kWarps; ++w) {
+          const uint32_t c = s.wsum[w] + s.wsum[kWarps + w];
+          total += c;
+          over |= c > static_cast<uint32_t>(kWarpCap);
+          cmax = max(cmax, s.wmax[w]);
+          if (csize > 1) cmax = max(cmax, s.wmax[kWarps + w]);
+        }
+        if (!over && total >= static_cast<uint32_t>(p.k)) {
+          const SrcPairs sp{s.data, s.data + kWarps * kWarpCap, s.wsum};
+          static_assert(kBins % kT == 0 && kBins <= 2048, "hist holds kBins bins");
+          const uint64_t thr = survivor_select(sp, p.k, tau, cmax, s);
+          emit(sp, thr, p, row, s);
+          done = true;
+        } else if (tid == 0) {
+          raise_error(p.err, kErrCapacity);
+        }
       }
     }
-    if (!done) {
+    if (!done && rank == 0) {
       // full-row radix select (also the exact redo of a missed cutoff)
       if (!cutoff && L <= kStage) {
         for (int i4 = tid; 4 * i4 < L; i4 += kT) {
@@ -588,21 +640,45 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
       }
     }
     __syncthreads();  // all emits done before the counter and the buffers are reused
+    if constexpr (kCsize > 1) cg::this_cluster().sync();  // rank 0 is done with the regions rank 1 refills
   }
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  if (a.R == 0) return cudaSuccess;
   const size_t smem = sizeof(TkSmem) + 16;
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   TkParams p{a.logits, a.ld,  a.row_len, a.R,          a.k,          a.col_blocks,
              a.nb,     a.block_size, a.out, a.force_path, dev.err_word};
-  const int grid = a.R < dev.sm_count ? a.R : dev.sm_count;
-  topk_kernel<<<grid, kT, smem, stream>>>(p);
-  return cudaGetLastError();
+  // Two CTAs per row while that leaves no row waiting for an SM and the rows
+  // can be long enough for the halved streaming pass to repay the cluster's
+  // costs: measured at 64 rows, k = 2048, the pair is ~2 us slower at 65536
+  // columns, even at 98304 and ~2 us faster at 131072.
+  const bool pair = 2 * a.R <= dev.sm_count && a.ld > 98304;
+  cudaError_t e = cudaFuncSetAttribute(pair ? topk_kernel<2> : topk_kernel<1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (!pair) {
+    const int grid = a.R < dev.sm_count ? a.R : dev.sm_count;
+    topk_kernel<1><<<grid, kT, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * a.R);
+  cfg.blockDim = dim3(kT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topk_kernel<2>, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace dsa

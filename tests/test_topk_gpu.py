@@ -92,3 +92,16 @@ def test_topk_cutoff_at_or_below_zero():
     for force in (0, 2):
         sel = gpu_topk(logits, ld, L, 2048, force_path=force)
         sets_equal(sel, logits, L, 2048)
+
+
+def test_topk_many_rows_one_cta_per_row():
+    """More rows than half the SM count: one CTA per row (the pair split of
+    the streaming pass is used only for fewer rows), mixed lengths so both the
+    staged and the cutoff path run."""
+    g = torch.Generator(device="cuda").manual_seed(6)
+    R, ld = 100, 70004
+    L = torch.randint(1, ld + 1, (R,), generator=g, device="cuda").to(torch.int32)
+    L[:4] = torch.tensor([ld, 2048, 16384, 40961], dtype=torch.int32, device="cuda")
+    logits = torch.randn(R, ld, generator=g, device="cuda")
+    sel = gpu_topk(logits, ld, L, 2048)
+    sets_equal(sel, logits, L, 2048)
