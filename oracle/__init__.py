@@ -233,3 +233,33 @@ def sparse_mla(q_bits, kv_bits, kv_page_stride, page_tokens, block_table, next_n
                            ctypes.c_double(scale), _p(rows), ctypes.c_int(len(rows)),
                            _p(out), _p(lse), ctypes.c_int(_threads(nthreads)))
     return out, lse
+
+
+def layer_sources(keep, mli):
+    """For each layer of a decode step, the layer whose indexer selection its
+    attention uses, following the Multi-layer Indexer abstract of the "JEV
+    Paper Radar" efficiency digest (2026-11-04):
+
+    * IndexCache: only the layers with keep[l] set run an indexer; a layer
+      without one reuses the selection of the latest earlier indexer layer;
+    * MLI (mli true): a layer attends the selection of the previous indexer
+      layer instead of its own, so its own indexer (if it keeps one) can run
+      concurrently with its attention.
+
+    Readings: "previous" means the latest indexer layer strictly before the
+    layer; the first layer has no previous one, so it must keep its indexer
+    and attends its own selection (the abstract does not say).  Plain Python
+    over a few layers: this is a schedule, not arithmetic."""
+    keep = [bool(x) for x in keep]
+    if not keep or not keep[0]:
+        raise ValueError("layer 0 must keep its indexer")
+    out = []
+    latest = -1  # the latest indexer layer before the current one
+    for layer, kept in enumerate(keep):
+        if mli and layer > 0:
+            out.append(latest)
+        else:
+            out.append(layer if kept else latest)
+        if kept:
+            latest = layer
+    return out

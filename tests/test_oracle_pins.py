@@ -431,3 +431,58 @@ def test_mla_no_valid_index():
     out, lse = oracle.sparse_mla(_bits(q), _bits(kv), 48, 4, perm.numpy(), 1,
                                  np.full((1, 4), -1, np.int32), 0.3, dv=8)
     assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+# ----------------------------------------------------- layer schedule (MLI) --
+def read_schedules(golden_dir):
+    out = []
+    with open(os.path.join(golden_dir, "layer_schedule.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kind, *kv = line.split()
+            d = dict(x.split("=") for x in kv)
+            out.append(([int(x) for x in d["keep"].split(",")], int(d["mli"]),
+                        [int(x) for x in d["src"].split(",")]))
+    return out
+
+
+def test_layer_sources_hand_worked(golden_dir):
+    cases = read_schedules(golden_dir)
+    assert len(cases) == 10
+    for keep, mli, src in cases:
+        assert oracle.layer_sources(keep, mli) == src, (keep, mli)
+
+
+def test_layer_sources_cumulative_max_form():
+    """The same rule written another way: the latest indexer layer at or
+    before l (sequential), or before l (MLI, first layer its own), as a
+    running maximum over the kept layer numbers."""
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        n = int(rng.integers(1, 17))
+        keep = rng.integers(0, 2, n)
+        keep[0] = 1
+        kept_at = np.where(keep == 1, np.arange(n), -1)
+        upto = np.maximum.accumulate(kept_at)            # latest kept j <= l
+        before = np.concatenate([[0], upto[:-1]])         # latest kept j < l
+        assert oracle.layer_sources(keep, False) == upto.tolist()
+        assert oracle.layer_sources(keep, True) == before.tolist()
+
+
+def test_layer_sources_invariants():
+    rng = np.random.default_rng(12)
+    for _ in range(100):
+        n = int(rng.integers(2, 12))
+        keep = rng.integers(0, 2, n)
+        keep[0] = 1
+        for mli in (False, True):
+            src = oracle.layer_sources(keep, mli)
+            for layer, j in enumerate(src):
+                assert keep[j] == 1                        # attends a real selection
+                assert j <= layer                          # never a later layer
+                if mli and layer > 0:
+                    assert j < layer                       # never its own (MLI)
+    with pytest.raises(ValueError):
+        oracle.layer_sources([0, 1, 1], False)
