@@ -46,6 +46,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+int set_last_error(int status, const char* msg) {
+  snprintf(g_msg, sizeof(g_msg), "%s", msg);
+  return status;
+}
+
 cudaError_t current_device_info(DeviceInfo* info) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);

@@ -19,6 +19,9 @@ struct DeviceInfo {
 // Fills `info` for the current device.
 cudaError_t current_device_info(DeviceInfo* info);
 
+// Sets this host thread's dsa_last_error() message; returns `status`.
+int set_last_error(int status, const char* msg);
+
 // Encodes a CUtensorMap through the driver entry point (no libcuda link).
 // dtype: 0 = uint8, 1 = bf16.  Returns false (and a message) on failure.
 bool encode_tensor_map(void* map_out, int dtype, int rank, void* base, const uint64_t* dims,

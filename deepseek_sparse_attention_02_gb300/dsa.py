@@ -49,6 +49,10 @@ _SIGS = {
     "dsa_candidate_expand": ([_P, _I, _I, _I, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "dsa_candidate_logits": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _I, _I, _P, _I, _I,
                               _P, _P, _SZ, _P, _I64, _P], _I),
+    "dsa_layer_sources": ([_P, _I, _I, _P], _I),
+    "dsa_decode_layers_workspace_size": ([_I, _I64, _I], _SZ),
+    "dsa_decode_layers": ([_P, _I, _P, _I, _I64, _I64, _I64, _I, _P, _I64, _P, _P, _I, _I, _I, _F,
+                           _I64, _P, _SZ, _P, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -178,3 +182,43 @@ def dsa_candidate_logits(q_fp8, q_scale, weights, k_fp4, k_page_stride, k_sf, sf
                                      _ptr(sparse_indices), nb, block_size, _ptr(end),
                                      _ptr(schedule), schedule_bytes, _ptr(logits), ld,
                                      _stream(stream)))
+
+
+
+class DsaLayer(ctypes.Structure):
+    """One record of dsa_decode_layers (struct dsa_layer of include/dsa.h)."""
+    _fields_ = [("q_fp8", _P), ("q_scale", _P), ("weights", _P), ("k_cache", _P),
+                ("k_scale", _P), ("q", _P), ("kv_cache", _P), ("out", _P), ("lse", _P)]
+
+
+def dsa_layer_sources(keep_indexer, mli: bool) -> list:
+    """Host-only: the layer whose selection each layer attends."""
+    n = len(keep_indexer)
+    keep = (ctypes.c_uint8 * n)(*[1 if x else 0 for x in keep_indexer])
+    src = (ctypes.c_int32 * n)()
+    _check(_lib.dsa_layer_sources(ctypes.cast(keep, _P), n, int(bool(mli)), ctypes.cast(src, _P)))
+    return list(src)
+
+
+def dsa_decode_layers_workspace_size(R: int, ld: int, k: int) -> int:
+    return int(_lib.dsa_decode_layers_workspace_size(R, ld, k))
+
+
+def dsa_decode_layers(layers, keep_indexer, mli, k_page_stride, s_page_stride, kv_page_stride,
+                      num_pages, block_table, ctx_len, row_len, num_req, next_n, k, sm_scale,
+                      ld, workspace, workspace_bytes, stream=None, side_stream=None):
+    """layers: a sequence of dicts with the dsa_layer fields (tensors, ints or
+    None); keep_indexer: a sequence of bools."""
+    n = len(layers)
+    recs = (DsaLayer * n)()
+    for i, L in enumerate(layers):
+        for f, _ in DsaLayer._fields_:
+            setattr(recs[i], f, _ptr(L.get(f)))
+    keep = (ctypes.c_uint8 * n)(*[1 if x else 0 for x in keep_indexer])
+    bt_stride = block_table.shape[1]
+    side = None if side_stream is None else _stream(side_stream)
+    _check(_lib.dsa_decode_layers(ctypes.cast(recs, _P), n, ctypes.cast(keep, _P), int(bool(mli)),
+                                  k_page_stride, s_page_stride, kv_page_stride, num_pages,
+                                  _ptr(block_table), bt_stride, _ptr(ctx_len), _ptr(row_len),
+                                  num_req, next_n, k, float(sm_scale), ld, _ptr(workspace),
+                                  workspace_bytes, _stream(stream), side))

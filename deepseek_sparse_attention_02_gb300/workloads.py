@@ -191,10 +191,17 @@ def _keys_by_page(layout: PagedLayout, seed, device, heavy_frac, heavy_shift, ch
 
 
 def make_indexer_case(ctx_lens, next_n=1, seed=0, device="cpu", shuffle=True,
-                      heavy_frac=0.05, heavy_shift=3.0, fmt="fp8") -> IndexerCase:
+                      heavy_frac=0.05, heavy_shift=3.0, fmt="fp8", layout=None) -> IndexerCase:
     """Paged indexer inputs for the dense (fmt='fp8') or candidate (fmt='mxfp4')
-    path."""
-    layout = make_layout(ctx_lens, seed, device="cpu", shuffle=shuffle)
+    path.  `layout` reuses the pages and block table of another case (as the
+    layers of one model share them); by default the seed draws a new one."""
+    if layout is None:
+        layout = make_layout(ctx_lens, seed, device="cpu", shuffle=shuffle)
+    else:
+        layout = PagedLayout(**{f: getattr(layout, f) for f in layout.__dataclass_fields__})
+        layout.ctx_len = layout.ctx_len.cpu()
+        layout.block_table = layout.block_table.cpu()
+        layout.pages_of = [p.cpu() for p in layout.pages_of]
     R = len(ctx_lens) * next_n
     qc, qs, w = _queries(R, seed, device)
     P = layout.num_pages

@@ -16,6 +16,9 @@
  *   b. candidate (sparse MQA) logits over MXFP4 keys        dsa_candidate_logits
  *   c. top-k over the candidate columns, mapped to tokens   dsa_topk (col_blocks)
  *
+ * and a multi-layer decode step with the IndexCache / Multi-layer Indexer
+ * selection schedules (JEV Paper Radar efficiency digest) dsa_decode_layers
+ *
  * Conventions for every entry point
  * ---------------------------------
  * - Pointers documented as "device" point to GPU memory of the current
@@ -262,6 +265,72 @@ dsa_status dsa_candidate_logits(const uint8_t* q_fp8, const float* q_scale, cons
                                 int next_n, const int32_t* sparse_indices, int nb,
                                 int block_size, const int32_t* end, const void* schedule,
                                 size_t schedule_bytes, float* logits, int64_t ld, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_decode_layers -- one decode step over several DSA layers with the
+ * cross-layer selection schedules of the Multi-layer Indexer (MLI) abstract
+ * ("JEV Paper Radar" efficiency digest, 2026-11-04):
+ *
+ *   IndexCache  only the layers with keep_indexer[l] != 0 run an indexer
+ *               (dsa_indexer_logits + dsa_topk); the others attend an earlier
+ *               layer's selection;
+ *   MLI         (mli != 0) every layer attends the selection of the previous
+ *               indexer layer instead of its own, which removes the dependency
+ *               of its attention on its own indexer: that indexer and its
+ *               top-k run on side_stream, concurrently with the attention.
+ *
+ * Layer l attends the selection of layer dsa_layer_sources(...)[l]: the
+ * latest indexer layer j <= l (mli = 0) or j < l (mli != 0; layer 0, which
+ * must keep its indexer, attends its own).  Each attention is one
+ * dsa_sparse_mla_decode of that layer's q and latent cache with that
+ * selection, so a layer's out / lse equal those of the three single calls
+ * made in the schedule's order.
+ *
+ *   layers[l]      host array of num_layers records (below); the indexer
+ *                  fields are read only for layers that keep an indexer.
+ *   keep_indexer   host [num_layers]; keep_indexer[0] must be set.
+ *   shared geometry: as dsa_indexer_logits (k_page_stride, s_page_stride,
+ *                  num_pages, block_table, bt_stride, ctx_len, num_req,
+ *                  next_n) and dsa_sparse_mla_decode (kv_page_stride,
+ *                  sm_scale); every layer's caches use the same block table.
+ *   row_len        device [R] int32: L_r of every query row (dsa_topk's row_len).
+ *   k              selected tokens per row (1 <= k <= DSA_MAX_TOPK).
+ *   ld             row stride of the logits scratch (>= max L_r, % 4 == 0).
+ *   workspace      device, dsa_decode_layers_workspace_size(R, ld, k) bytes:
+ *                  the logits, two selection buffers, the MLA split partials.
+ *   stream         the step's stream: the attentions (and layer 0's indexer)
+ *                  run on it, and it waits at the end for everything the call
+ *                  put on side_stream.
+ *   side_stream    a second stream for MLI's indexers, or NULL (then they run
+ *                  on `stream`, with the same results and no overlap).
+ * The call records and waits on CUDA events it creates once per host thread
+ * and device.  All arguments are checked before anything is enqueued.
+ * ---------------------------------------------------------------------- */
+typedef struct dsa_layer {
+  const uint8_t* q_fp8;     /* [R, 64, 128] e4m3 indexer query            */
+  const float* q_scale;     /* [R, 64]                                    */
+  const float* weights;     /* [R, 64]                                    */
+  const uint8_t* k_cache;   /* the layer's FP8 key pages                  */
+  const uint8_t* k_scale;   /* the layer's per-token key scales           */
+  const uint16_t* q;        /* [R, 128, 576] bf16 attention query          */
+  const uint16_t* kv_cache; /* the layer's latent pages                    */
+  uint16_t* out;            /* [R, 128, 512] bf16                          */
+  float* lse;               /* [R, 128] f32, or NULL                       */
+} dsa_layer;
+
+/* Host-only: src[l] = the layer whose selection layer l attends under the
+ * schedule above.  DSA_ERR_INVALID_ARG if keep_indexer[0] == 0. */
+dsa_status dsa_layer_sources(const uint8_t* keep_indexer, int num_layers, int mli, int32_t* src);
+
+size_t dsa_decode_layers_workspace_size(int R, int64_t ld, int k);
+
+dsa_status dsa_decode_layers(const dsa_layer* layers, int num_layers,
+                             const uint8_t* keep_indexer, int mli, int64_t k_page_stride,
+                             int64_t s_page_stride, int64_t kv_page_stride, int num_pages,
+                             const int32_t* block_table, int64_t bt_stride,
+                             const int32_t* ctx_len, const int32_t* row_len, int num_req,
+                             int next_n, int k, float sm_scale, int64_t ld, void* workspace,
+                             size_t workspace_bytes, void* stream, void* side_stream);
 
 #ifdef __cplusplus
 }
