@@ -202,6 +202,62 @@ def candidate_kernels(st):
     return ks
 
 
+LAYER_SCHEDULES = [(1, False), (1, True), (2, False), (2, True), (4, False), (4, True)]
+
+
+def build_layers(st, n_layers=8):
+    """A decode step over n_layers DSA layers for the IndexCache / Multi-layer
+    Indexer schedules: every layer has its own indexer and attention queries;
+    all read the headline workload's key and latent caches (each far larger
+    than L2, so sharing them changes no traffic)."""
+    import torch
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case, R, dev = st["case"], st["R"], st["L"].device
+    c = case.cache
+    layers = []
+    for l in range(n_layers):
+        qc, qs, w = W.make_index_queries(R, seed=100 + l, device=dev)
+        layers.append(dict(q_fp8=qc, q_scale=qs, weights=w, k_cache=c,
+                           k_scale=c.data_ptr() + W.FP8_KEY_BYTES,
+                           q=W.make_mla_queries(R, seed=200 + l, device=dev), kv_cache=st["mla"].kv,
+                           out=torch.empty((R, W.MLA_HEADS, W.MLA_DV), dtype=torch.bfloat16,
+                                           device=dev),
+                           lse=torch.empty((R, W.MLA_HEADS), device=dev)))
+    wsb = dsa.dsa_decode_layers_workspace_size(R, st["ld"], TOPK)
+    return dict(layers=layers, wsb=wsb, ws=torch.empty(wsb, dtype=torch.uint8, device=dev),
+                side=torch.cuda.Stream(device=dev))
+
+
+def time_layers(st, lst, steps, warmup, stream):
+    """ms per multi-layer step for each (retention 1/r, MLI) schedule."""
+    import torch
+    from deepseek_sparse_attention_02_gb300 import dsa
+    lay = st["case"].layout
+    n = len(lst["layers"])
+    res, launches = {}, 0
+    for r, mli in LAYER_SCHEDULES:
+        keep = [l % r == 0 for l in range(n)]
+
+        def step():
+            dsa.dsa_decode_layers(lst["layers"], keep, mli, 8448, 8448, 64 * 576 * 2,
+                                  lay.num_pages, lay.block_table, lay.ctx_len, st["L"],
+                                  len(lay.ctx_len), 2, TOPK, st["mla"].scale, st["ld"],
+                                  lst["ws"], lst["wsb"], stream=stream, side_stream=lst["side"])
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        res[f"r{r}_{'mli' if mli else 'seq'}"] = a.elapsed_time(b) / steps
+        launches += steps * (2 * sum(keep) + n * (1 + (1 if st["wsb"] > 0 else 0)))
+    return res, launches
+
+
 def time_kernels(kernels, steps, warmup, stream):
     """Runs `steps` timed passes; returns (total ms, {name: mean ms per launch})."""
     import torch
@@ -349,6 +405,7 @@ def run_ours(args):
     kernels = decode_kernels(st)
     cst = None if args.no_candidate else build_candidate(device)
     ckernels = [] if cst is None else candidate_kernels(cst)
+    lst = None if args.no_layers else build_layers(st)
     torch.cuda.synchronize()
 
     barrier(pg, device)
@@ -356,6 +413,8 @@ def run_ours(args):
         total_ms, per = time_kernels(kernels, args.steps, args.warmup, stream)
         if ckernels:
             c_total_ms, c_per = time_kernels(ckernels, args.steps, args.warmup, stream)
+        if lst is not None:
+            lay_ms, lay_launches = time_layers(st, lst, args.steps, args.warmup, stream)
     barrier(pg, device)
     torch.cuda.synchronize()
     assert dsa.dsa_get_device_error() == 0, "device error word set during the benchmark"
@@ -393,6 +452,17 @@ def run_ours(args):
                 "logits_hbm_gbs": c_bytes / (c_log * 1e-3) / 1e9,
                 "topk_rows_per_s": cst["R"] / (ctk * 1e-3)}
 
+    layers = None
+    if lst is not None:
+        base = lay_ms["r1_seq"]
+        layers = {"workload": f"{len(lst['layers'])} DSA layers of the headline step (own "
+                              "indexer and attention queries per layer, shared caches); "
+                              "retention 1/r keeps the indexer of layers l % r == 0; "
+                              "mli = each layer attends the previous indexer layer's "
+                              "selection, its own indexer on a second stream",
+                  "ms_per_step": {k: round(v, 4) for k, v in lay_ms.items()},
+                  "speedup_vs_r1_seq": {k: round(base / v, 3) for k, v in lay_ms.items()}}
+
     line = {
         "metric": METRIC,
         "value": value,
@@ -422,12 +492,14 @@ def run_ours(args):
                        "gather_gbs": R * TOPK * 1152 / (per["sparse_mla"] * 1e-3) / 1e9,
                        "tflops": R * 2 * 128 * TOPK * (576 + 512) / (per["sparse_mla"] * 1e-3) / 1e12},
         "candidate_path": cand,
+        "layer_schedules": layers,
         "roofline": {"kernel": "dsa_indexer_logits", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": peak_src,
                      "alg_bytes_per_launch": alg_bytes},
         "gpu_launches": args.steps * (len(kernels) + (1 if st["wsb"] > 0 else 0)) +
-                        (args.steps * (len(ckernels) + 1) if ckernels else 0),
+                        (args.steps * (len(ckernels) + 1) if ckernels else 0) +
+                        (lay_launches if lst is not None else 0),
         "e2e": {"value": world * keys_per_step / (e2e_ms * 1e-3), "unit": "keys/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
@@ -484,6 +556,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--requests", type=int, default=32,
                     help="decode requests (32 = the 128K workload; fewer for profiling)")
+    ap.add_argument("--no-layers", action="store_true",
+                    help="skip the multi-layer IndexCache / MLI schedule measurement")
     ap.add_argument("--no-candidate", action="store_true",
                     help="skip the candidate-path leg (profiling)")
     args = ap.parse_args()

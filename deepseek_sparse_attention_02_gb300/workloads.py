@@ -257,6 +257,18 @@ class MLACase:
     scale: float
 
 
+def make_index_queries(R, seed=0, device="cpu"):
+    """Indexer queries of another layer over the same cache: (e4m3 codes
+    [R, 64, 128], per-head scales [R, 64], head weights [R, 64])."""
+    return _queries(R, seed, device)
+
+
+def make_mla_queries(R, seed=0, device="cpu"):
+    """Attention queries [R, 128, 576] bf16 of another layer."""
+    g = _gen(seed * 49979687 + 13, device)
+    return torch.randn(R, MLA_HEADS, MLA_DQK, generator=g, device=device).to(torch.bfloat16)
+
+
 def make_mla_case(R, num_pages, seed=0, device="cpu", chunk_pages=2048) -> MLACase:
     g = _gen(seed * 49979687 + 11, device)
     q = torch.randn(R, MLA_HEADS, MLA_DQK, generator=g, device=device).to(torch.bfloat16)
