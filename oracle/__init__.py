@@ -151,9 +151,23 @@ def indexer_logits(q, q_scale, w, k_cache, k_page_stride, k_scale_bytes,
     return out, mag
 
 
-def candidate_expand(cand, bs, ctx_len, next_n):
-    """Sorted candidate blocks and the valid sparse-column count per row."""
+def candidate_expand(cand, bs, ctx_len, next_n, sparse_bs=None):
+    """Sorted candidate blocks and the valid sparse-column count per row.
+
+    With sparse_bs (a divisor of bs; the vLLM ``sparse_indexer`` builder's
+    ``sparse_block_kv``, which makes ``num_sparse_blocks = candidate_topk_blocks
+    * (candidate_block_size // sparse_block_kv)``), candidate block b of bs
+    tokens is first written as its m = bs / sparse_bs consecutive sparse blocks
+    b*m .. b*m+m-1 of sparse_bs tokens; the result is then over those."""
     cand = np.ascontiguousarray(cand, np.int32)
+    if sparse_bs is not None and sparse_bs != bs:
+        if sparse_bs <= 0 or bs % sparse_bs:
+            raise ValueError("sparse_bs must divide the candidate block size")
+        m = bs // sparse_bs
+        R0, nb0 = cand.shape
+        cand = (cand.astype(np.int64)[:, :, None] * m + np.arange(m)).reshape(R0, nb0 * m)
+        cand = np.ascontiguousarray(cand, np.int32)
+        bs = sparse_bs
     R, nb = cand.shape
     ctx = np.ascontiguousarray(ctx_len, np.int32)
     si = np.empty_like(cand)

@@ -276,6 +276,27 @@ def test_candidate_expand_brute_force():
         assert all(valid[:end[r]]) and not any(valid[end[r]:])
 
 
+def test_candidate_expand_sparse_blocks_brute_force():
+    """Candidate blocks of cbs tokens scored as sparse blocks of sbs tokens
+    (cbs a multiple of sbs): the sparse columns must cover exactly the
+    candidate blocks' tokens, in ascending token order, the valid ones first;
+    the sparse block count is nb * cbs / sbs."""
+    rng = np.random.default_rng(8)
+    for cbs, sbs in ((8, 4), (12, 4), (16, 2), (6, 6)):
+        nb = 5
+        ctx = np.array([37, 9, 80, 1], np.int32)
+        cand = np.stack([rng.permutation(10)[:nb] for _ in range(4)]).astype(np.int32)
+        si, end = oracle.candidate_expand(cand, cbs, ctx, 1, sparse_bs=sbs)
+        assert si.shape == (4, nb * cbs // sbs)
+        for r in range(4):
+            want = sorted(b * cbs + o for b in cand[r].tolist() for o in range(cbs))
+            got = [int(si[r, c // sbs]) * sbs + c % sbs for c in range(si.shape[1] * sbs)]
+            assert got == want
+            assert end[r] == sum(1 for t in want if t < ctx[r])
+    with pytest.raises(ValueError):
+        oracle.candidate_expand(cand, 8, ctx, 1, sparse_bs=3)
+
+
 def _mxfp4_keys(rng, T, D):
     nib = rng.integers(0, 16, size=(T, D)).astype(np.uint8)
     packed = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
