@@ -18,6 +18,8 @@
 // kind::f8f6f4 MMA per 32-element scale group (K = 32) into four TMEM
 // accumulators, so the epilogue applies the UE8M0 scales exactly:
 //   logit = sum_h w'_h * ReLU(sum_g 2^(e_g - 127) * D_g[h]).
+#include <cuda_bf16.h>
+
 #include <cstdio>
 
 #include "internal.h"
@@ -49,8 +51,18 @@ __global__ void __launch_bounds__(256) candidate_expand_kernel(CandExpandArgs a,
   const int tid = threadIdx.x;
   int n2 = 1;
   while (n2 < a.nb) n2 <<= 1;
-  const int32_t* src = a.cand + static_cast<int64_t>(r) * a.nb;
-  for (int i = tid; i < n2; i += 256) ids[i] = i < a.nb ? src[i] : 0x7fffffff;
+  // candidate block b covers the sparse blocks b*expand .. b*expand+expand-1;
+  // ids past int32 range stay past the context (they sort last)
+  const int m = a.expand;
+  const int32_t* src = a.cand + static_cast<int64_t>(r) * (a.nb / m);
+  for (int i = tid; i < n2; i += 256) {
+    int v = 0x7fffffff;
+    if (i < a.nb) {
+      const int64_t b = static_cast<int64_t>(src[i / m]) * m + i % m;
+      v = b > 0x7ffffffell ? 0x7fffffff : static_cast<int>(b);
+    }
+    ids[i] = v;
+  }
   __syncthreads();
   for (int size = 2; size <= n2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -148,7 +160,8 @@ struct CParams {
   int nb;
   const int32_t* end;
   const int32_t* sched;  // [R+1] exclusive chunk prefix
-  float* logits;
+  float* logits;          // f32 output, or
+  uint16_t* logits_bf16;  // bf16 output (round to nearest even) when not null
   int64_t ld;
   uint32_t* err;
 };
@@ -492,7 +505,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.tempty[wg]);
         const int col = t * kTileCols + tr;
-        if (col < endr) p.logits[static_cast<int64_t>(r) * p.ld + col] = acc[0] + acc[1];
+        if (col < endr) {
+          const int64_t o = static_cast<int64_t>(r) * p.ld + col;
+          if (p.logits_bf16)
+            p.logits_bf16[o] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[0] + acc[1]));
+          else
+            p.logits[o] = acc[0] + acc[1];
+        }
       }
       if (bad) break;
       // A warp may walk through a group without processing any of its tiles (they
@@ -559,6 +578,7 @@ cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& d
   p.end = a.end;
   p.sched = static_cast<const int32_t*>(a.schedule);
   p.logits = a.logits;
+  p.logits_bf16 = a.logits_bf16;
   p.ld = a.ld;
   p.err = dev.err_word;
   // at least 120 KB so that one CTA (holding all 512 TMEM columns) runs per SM

@@ -131,6 +131,77 @@ dsa_status cuda_status(cudaError_t e, const char* what) {
   return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// dsa_topk / dsa_topk_bf16: the checks and the launch, for f32 or bf16 scores.
+dsa_status topk_impl(const char* fn, const void* logits, bool bf16, int64_t ld,
+                     const int32_t* row_len, int R, int k, const int32_t* col_blocks, int nb,
+                     int block_size, int32_t* out_idx, int force_path, void* stream) {
+  if (!logits || !row_len || !out_idx)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (R < 0 || k < 1 || k > DSA_MAX_TOPK || ld < 4 || ld % 4 || !aligned16(logits))
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: need R >= 0, 1 <= k <= %d, ld %% 4 == 0, 16-byte aligned logits", fn,
+                DSA_MAX_TOPK);
+  if (ld > (1ll << 31) - 1) return fail(DSA_ERR_UNSUPPORTED, "%s: rows longer than 2^31", fn);
+  if (col_blocks && (nb < 1 || block_size < 1))
+    return fail(DSA_ERR_INVALID_ARG, "%s: col_blocks needs nb >= 1 and block_size >= 1", fn);
+  if (force_path < 0 || force_path > 2)
+    return fail(DSA_ERR_INVALID_ARG, "%s: force_path must be 0, 1 or 2", fn);
+  if (R == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  TopkArgs a{logits, ld, row_len, R, k, col_blocks, nb, block_size, out_idx, force_path,
+             bf16 ? 1 : 0};
+  return cuda_status(launch_topk(a, dev, static_cast<cudaStream_t>(stream)), fn);
+}
+
+// dsa_candidate_logits / _bf16: the checks and the launch; exactly one of
+// logits32 / logits16 is the output.
+dsa_status cand_logits_impl(const char* fn, const uint8_t* q_fp8, const float* q_scale,
+                            const float* weights, const uint8_t* k_fp4, int64_t k_page_stride,
+                            const uint8_t* k_sf, int64_t sf_page_stride, int num_pages,
+                            const int32_t* block_table, int64_t bt_stride, int num_req,
+                            int next_n, const int32_t* sparse_indices, int nb, int block_size,
+                            const int32_t* end, const void* schedule, size_t schedule_bytes,
+                            float* logits32, uint16_t* logits16, int64_t ld, void* stream) {
+  const void* logits = logits32 ? static_cast<const void*>(logits32) : logits16;
+  if (!q_fp8 || !q_scale || !weights || !k_fp4 || !k_sf || !block_table || !sparse_indices ||
+      !end || !schedule || !logits)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (num_req < 0 || next_n < 1 || num_pages < 1 || bt_stride < 1 || nb < 1)
+    return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes", fn);
+  if (block_size != DSA_PAGE_TOKENS)
+    return fail(DSA_ERR_UNSUPPORTED,
+                "%s: the sparse block size must equal the %d-token page (got %d)", fn,
+                DSA_PAGE_TOKENS, block_size);
+  if (k_page_stride < 64 * 64 || k_page_stride % 16 || sf_page_stride < 256 ||
+      sf_page_stride % 16 || !aligned16(k_fp4) || !aligned16(k_sf) || !aligned16(q_fp8) ||
+      !aligned16(logits) || ld % 4 || ld < static_cast<int64_t>(nb) * block_size)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: strides must be multiples of 16, buffers 16-byte aligned, ld >= nb*bs and "
+                "ld %% 4 == 0",
+                fn);
+  const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
+  if (R64 > (1 << 20)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
+  const int R = static_cast<int>(R64);
+  if (schedule_bytes < candidate_schedule_size(R))
+    return fail(DSA_ERR_WORKSPACE, "%s: schedule needs %zu bytes", fn,
+                candidate_schedule_size(R));
+  if (R == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  CandLogitsArgs a{q_fp8,          q_scale,   weights,     k_fp4,     k_page_stride, k_sf,
+                   sf_page_stride, num_pages, block_table, bt_stride, num_req,       next_n,
+                   sparse_indices, nb,        block_size,  end,       schedule,      logits32,
+                   logits16,       ld};
+  char msg[256] = "";
+  cudaError_t e =
+      launch_candidate_logits(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
+  if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
+  return cuda_status(e, fn);
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -201,24 +272,15 @@ dsa_status dsa_indexer_logits(const uint8_t* q_fp8, const float* q_scale, const 
 dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
                     const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
                     int force_path, void* stream) {
-  const char* fn = "dsa_topk";
-  if (!logits || !row_len || !out_idx)
-    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
-  if (R < 0 || k < 1 || k > DSA_MAX_TOPK || ld < 4 || ld % 4 || !aligned16(logits))
-    return fail(DSA_ERR_INVALID_ARG,
-                "%s: need R >= 0, 1 <= k <= %d, ld %% 4 == 0, 16-byte aligned logits", fn,
-                DSA_MAX_TOPK);
-  if (ld > (1ll << 31) - 1) return fail(DSA_ERR_UNSUPPORTED, "%s: rows longer than 2^31", fn);
-  if (col_blocks && (nb < 1 || block_size < 1))
-    return fail(DSA_ERR_INVALID_ARG, "%s: col_blocks needs nb >= 1 and block_size >= 1", fn);
-  if (force_path < 0 || force_path > 2)
-    return fail(DSA_ERR_INVALID_ARG, "%s: force_path must be 0, 1 or 2", fn);
-  if (R == 0) return ok();
-  DeviceInfo dev;
-  dsa_status st = device_ready(&dev);
-  if (st != DSA_OK) return st;
-  TopkArgs a{logits, ld, row_len, R, k, col_blocks, nb, block_size, out_idx, force_path};
-  return cuda_status(launch_topk(a, dev, static_cast<cudaStream_t>(stream)), fn);
+  return dsa::topk_impl("dsa_topk", logits, false, ld, row_len, R, k, col_blocks, nb, block_size,
+                        out_idx, force_path, stream);
+}
+
+dsa_status dsa_topk_bf16(const uint16_t* logits, int64_t ld, const int32_t* row_len, int R, int k,
+                         const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
+                         int force_path, void* stream) {
+  return dsa::topk_impl("dsa_topk_bf16", logits, true, ld, row_len, R, k, col_blocks, nb,
+                        block_size, out_idx, force_path, stream);
 }
 
 size_t dsa_sparse_mla_workspace_size(int R, int k) {
@@ -276,11 +338,14 @@ dsa_status dsa_candidate_expand(const int32_t* cand, int R, int nb, int block_si
     return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
   if (R < 0 || nb < 1 || next_n < 1 || (R % next_n) != 0)
     return fail(DSA_ERR_INVALID_ARG, "%s: need nb >= 1, next_n >= 1, R %% next_n == 0", fn);
-  if (block_size != DSA_PAGE_TOKENS)
+  if (block_size < DSA_PAGE_TOKENS || block_size % DSA_PAGE_TOKENS ||
+      block_size > 64 * DSA_PAGE_TOKENS)
     return fail(DSA_ERR_UNSUPPORTED,
-                "%s: candidate_block_size must equal the %d-token page (got %d)", fn,
+                "%s: candidate_block_size must be 1..64 times the %d-token page (got %d)", fn,
                 DSA_PAGE_TOKENS, block_size);
-  if (nb > 4096) return fail(DSA_ERR_UNSUPPORTED, "%s: nb > 4096 candidate blocks", fn);
+  const int expand = block_size / DSA_PAGE_TOKENS;
+  if (static_cast<int64_t>(nb) * expand > 4096)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: more than 4096 sparse blocks per row", fn);
   if (schedule_bytes < candidate_schedule_size(R))
     return fail(DSA_ERR_WORKSPACE, "%s: schedule needs %zu bytes", fn,
                 candidate_schedule_size(R));
@@ -288,7 +353,8 @@ dsa_status dsa_candidate_expand(const int32_t* cand, int R, int nb, int block_si
   DeviceInfo dev;
   dsa_status st = device_ready(&dev);
   if (st != DSA_OK) return st;
-  CandExpandArgs a{cand, R, nb, block_size, ctx_len, next_n, sparse_indices, end, schedule};
+  CandExpandArgs a{cand,    R,      nb * expand,    DSA_PAGE_TOKENS, expand,
+                   ctx_len, next_n, sparse_indices, end,             schedule};
   return cuda_status(launch_candidate_expand(a, dev, static_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -299,44 +365,26 @@ dsa_status dsa_candidate_logits(const uint8_t* q_fp8, const float* q_scale, cons
                                 int next_n, const int32_t* sparse_indices, int nb,
                                 int block_size, const int32_t* end, const void* schedule,
                                 size_t schedule_bytes, float* logits, int64_t ld, void* stream) {
-  const char* fn = "dsa_candidate_logits";
-  if (!q_fp8 || !q_scale || !weights || !k_fp4 || !k_sf || !block_table || !sparse_indices ||
-      !end || !schedule || !logits)
-    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
-  if (num_req < 0 || next_n < 1 || num_pages < 1 || bt_stride < 1 || nb < 1)
-    return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes", fn);
-  if (block_size != DSA_PAGE_TOKENS)
-    return fail(DSA_ERR_UNSUPPORTED,
-                "%s: candidate_block_size must equal the %d-token page (got %d)", fn,
-                DSA_PAGE_TOKENS, block_size);
-  if (k_page_stride < 64 * 64 || k_page_stride % 16 || sf_page_stride < 256 ||
-      sf_page_stride % 16 || !aligned16(k_fp4) || !aligned16(k_sf) || !aligned16(q_fp8) ||
-      !aligned16(logits) || ld % 4 || ld < static_cast<int64_t>(nb) * block_size)
-    return fail(DSA_ERR_INVALID_ARG,
-                "%s: strides must be multiples of 16, buffers 16-byte aligned, ld >= nb*bs and "
-                "ld %% 4 == 0",
-                fn);
-  const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
-  if (R64 > (1 << 20)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
-  const int R = static_cast<int>(R64);
-  if (schedule_bytes < candidate_schedule_size(R))
-    return fail(DSA_ERR_WORKSPACE, "%s: schedule needs %zu bytes", fn,
-                candidate_schedule_size(R));
-  if (R == 0) return ok();
-  DeviceInfo dev;
-  dsa_status st = device_ready(&dev);
-  if (st != DSA_OK) return st;
-  CandLogitsArgs a{q_fp8,          q_scale,   weights,     k_fp4,     k_page_stride, k_sf,
-                   sf_page_stride, num_pages, block_table, bt_stride, num_req,       next_n,
-                   sparse_indices, nb,        block_size,  end,       schedule,      logits,
-                   ld};
-  char msg[256] = "";
-  cudaError_t e =
-      launch_candidate_logits(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
-  if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
-  return cuda_status(e, fn);
+  return dsa::cand_logits_impl("dsa_candidate_logits", q_fp8, q_scale, weights, k_fp4,
+                               k_page_stride, k_sf, sf_page_stride, num_pages, block_table,
+                               bt_stride, num_req, next_n, sparse_indices, nb, block_size, end,
+                               schedule, schedule_bytes, logits, nullptr, ld, stream);
 }
 
+dsa_status dsa_candidate_logits_bf16(const uint8_t* q_fp8, const float* q_scale,
+                                     const float* weights, const uint8_t* k_fp4,
+                                     int64_t k_page_stride, const uint8_t* k_sf,
+                                     int64_t sf_page_stride, int num_pages,
+                                     const int32_t* block_table, int64_t bt_stride, int num_req,
+                                     int next_n, const int32_t* sparse_indices, int nb,
+                                     int block_size, const int32_t* end, const void* schedule,
+                                     size_t schedule_bytes, uint16_t* logits, int64_t ld,
+                                     void* stream) {
+  return dsa::cand_logits_impl("dsa_candidate_logits_bf16", q_fp8, q_scale, weights, k_fp4,
+                               k_page_stride, k_sf, sf_page_stride, num_pages, block_table,
+                               bt_stride, num_req, next_n, sparse_indices, nb, block_size, end,
+                               schedule, schedule_bytes, nullptr, logits, ld, stream);
+}
 
 size_t dsa_sparse_mla_static_scratch_bytes(void) { return mla_static_scratch_bytes(); }
 

@@ -50,7 +50,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, const DeviceInfo& dev, cudaStre
                            char* msg, size_t msg_len);
 
 struct TopkArgs {
-  const float* logits;
+  const void* logits;  // f32, or bf16 when bf16 != 0
   int64_t ld;
   const int32_t* row_len;
   int R;
@@ -60,6 +60,7 @@ struct TopkArgs {
   int block_size;
   int32_t* out;
   int force_path;
+  int bf16;
 };
 
 cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream);
@@ -93,10 +94,11 @@ cudaError_t launch_sparse_mla_static(const MlaArgs& a, const DeviceInfo& dev, cu
                                      size_t* need);
 
 struct CandExpandArgs {
-  const int32_t* cand;
+  const int32_t* cand;  // [R, nb_cand] candidate block ids
   int R;
-  int nb;
-  int bs;
+  int nb;      // sparse blocks per row = nb_cand * expand
+  int bs;      // sparse block size (the 64-token page)
+  int expand;  // sparse blocks per candidate block
   const int32_t* ctx_len;
   int next_n;
   int32_t* sparse_indices;
@@ -126,7 +128,8 @@ struct CandLogitsArgs {
   int bs;
   const int32_t* end;
   const void* schedule;
-  float* logits;
+  float* logits;         // f32 output, or
+  uint16_t* logits_bf16; // bf16 output (round to nearest even) when not null
   int64_t ld;
 };
 

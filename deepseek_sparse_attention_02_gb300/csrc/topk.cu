@@ -47,7 +47,7 @@ constexpr int kSample = 8 * kGroups;
 static_assert(kSample / 4 <= kT, "the sample is loaded as one float4 per thread");
 
 struct TkParams {
-  const float* logits;
+  const void* logits;  // f32 or bf16 [R, ld]
   int64_t ld;
   const int32_t* row_len;
   int R;
@@ -132,21 +132,51 @@ __device__ __forceinline__ float ldg_nc(const float* ptr) {
   return v;
 }
 
+// A row of scores in global memory: f32, or bf16 widened to f32 on load (an
+// exact widening, so a bf16 row selects as the f32 row of the same values).
+// load4 needs e0 % 4 == 0 (16- or 8-byte aligned loads).
+template <class T>
+struct RowPtr;
+template <>
+struct RowPtr<float> {
+  const float* p;
+  __device__ float4 load4(int64_t e0) const { return ldg_nc4(p + e0); }
+  __device__ float load1(int64_t e) const { return ldg_nc(p + e); }
+  __device__ RowPtr offset(int64_t c) const { return {p + c}; }
+};
+template <>
+struct RowPtr<uint16_t> {
+  const uint16_t* p;
+  __device__ float4 load4(int64_t e0) const {
+    uint32_t a, b;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "l"(p + e0));
+    return make_float4(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u),
+                       __uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
+  }
+  __device__ float load1(int64_t e) const {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p + e));
+    return __uint_as_float(static_cast<uint32_t>(v) << 16);
+  }
+  __device__ RowPtr offset(int64_t c) const { return {p + c}; }
+};
+
 // Element sources.  visit(f) calls f(key, ~col, valid) with every lane of a
 // warp taking part in each call (valid = false for padding lanes).
 
+template <class T>
 struct SrcGlobal {  // the row [0, n), read from global memory
-  const float* row;
+  RowPtr<T> row;
   int n;
   static constexpr int kB = 4;  // float4 loads in flight per thread
   __device__ float4 load4(int e0) const {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (e0 + 3 < n) {
-      v = ldg_nc4(row + e0);
+      v = row.load4(e0);
     } else if (e0 < n) {
-      v.x = row[e0];
-      if (e0 + 1 < n) v.y = row[e0 + 1];
-      if (e0 + 2 < n) v.z = row[e0 + 2];
+      v.x = row.load1(e0);
+      if (e0 + 1 < n) v.y = row.load1(e0 + 1);
+      if (e0 + 2 < n) v.z = row.load1(e0 + 2);
     }
     return v;
   }
@@ -403,8 +433,8 @@ __device__ uint32_t local_tau(const uint32_t* sample, int n, uint32_t q, uint32_
 // key_of(x) >= tau is exactly the signed compare of x's bits with tau's float
 // bits (negative values, -0.0 and -NaN fall below, +NaN above, as in key_of):
 // one instruction per element.
-template <bool kPositiveTau, bool kTop>
-__device__ void compact(const SrcGlobal& g, uint32_t col0, uint32_t tau, uint32_t* keys,
+template <bool kPositiveTau, bool kTop, class T>
+__device__ void compact(const SrcGlobal<T>& g, uint32_t col0, uint32_t tau, uint32_t* keys,
                         uint32_t* cols, uint32_t* wsum, uint32_t* wmax) {
   constexpr int kB = 4;  // float4 loads per batch
   const int n = g.n;
@@ -454,7 +484,7 @@ __device__ void compact(const SrcGlobal& g, uint32_t col0, uint32_t tau, uint32_
       const int bit = __ffs(mask) - 1;
       mask &= mask - 1;
       const int e = 4 * (base + (bit >> 2) * kT + threadIdx.x) + (bit & 3);
-      const uint32_t key = key_of(ldg_nc(g.row + e));
+      const uint32_t key = key_of(g.row.load1(e));
       kmax = max(kmax, key);
       if (pos < static_cast<uint32_t>(kWarpCap)) {
         const uint32_t j = kTop ? kWarpCap - 1 - pos : pos;
@@ -504,7 +534,7 @@ __device__ void emit(const Src& src, uint64_t thr, const TkParams& p, int row, T
 // kCsize = CTAs per row: 1, or 2 (a cluster).  The two are separate kernels:
 // measured on GB300, merely containing cluster instructions cost the one-CTA
 // kernel ~2 us per launch.
-template <int kCsize>
+template <int kCsize, class T>
 __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
   extern __shared__ uint8_t smem_raw[];
   TkSmem& s =
@@ -522,7 +552,7 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
   TkSmem& s0 = *s0p;
 
   for (int row = blockIdx.x / csize; row < p.R; row += gridDim.x / csize) {
-    const float* rowp = p.logits + static_cast<int64_t>(row) * p.ld;
+    const RowPtr<T> rowp{static_cast<const T*>(p.logits) + static_cast<int64_t>(row) * p.ld};
     int L = p.row_len[row];
     if (L < 0) L = 0;
     if (L > p.ld) {
@@ -557,13 +587,13 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
           // float4 tid of the sample: group tid / 2, half tid % 2
           const int64_t g0 =
               ((static_cast<int64_t>(tid >> 1) * (L - 8)) / (kGroups - 1)) & ~3ll;
-          const float4 v = ldg_nc4(rowp + g0 + 4 * (tid & 1));
+          const float4 v = rowp.load4(g0 + 4 * (tid & 1));
           *reinterpret_cast<uint4*>(s.sample + 4 * tid) =
               make_uint4(key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w));
         }
       } else {
         ns = L;
-        for (int i = tid; i < L; i += kT) s.sample[i] = key_of(ldg_nc(rowp + i));
+        for (int i = tid; i < L; i += kT) s.sample[i] = key_of(rowp.load1(i));
       }
       __syncthreads();
       // q = ceil(2k ns / L) sample keys above tau (integer arithmetic: FP64 is
@@ -577,7 +607,7 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
       const int h = csize > 1 ? ((L + 7) >> 3) << 2 : L;
       const int c0 = rank == 0 ? 0 : h;
       const int c1 = rank == 0 ? h : L;
-      const SrcGlobal g{rowp + c0, c1 - c0};
+      const SrcGlobal<T> g{rowp.offset(c0), c1 - c0};
       uint32_t* const kw = s.data;
       uint32_t* const cw = s.data + kWarps * kWarpCap;
       if (rank == 0) {  // this CTA's shared memory, filled from the bottom
@@ -622,11 +652,11 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
         for (int i4 = tid; 4 * i4 < L; i4 += kT) {
           const int e0 = 4 * i4;
           if (e0 + 3 < L) {
-            const float4 v = ldg_nc4(rowp + e0);
+            const float4 v = rowp.load4(e0);
             *reinterpret_cast<uint4*>(s.data + e0) =
                 make_uint4(key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w));
           } else {
-            for (int j = e0; j < L; ++j) s.data[j] = key_of(rowp[j]);
+            for (int j = e0; j < L; ++j) s.data[j] = key_of(rowp.load1(j));
           }
         }
         __syncthreads();
@@ -634,7 +664,7 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
         const uint64_t thr = radix_select(ss, p.k, Sel{0, 0, 0u, 0u}, s);
         emit(ss, thr, p, row, s);
       } else {
-        const SrcGlobal g{rowp, L};
+        const SrcGlobal<T> g{rowp, L};
         const uint64_t thr = radix_select(g, p.k, Sel{0, 0, 0u, 0u}, s);
         emit(g, thr, p, row, s);
       }
@@ -646,8 +676,10 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  if (a.R == 0) return cudaSuccess;
+namespace {
+
+template <class T>
+cudaError_t launch_topk_t(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   const size_t smem = sizeof(TkSmem) + 16;
   TkParams p{a.logits, a.ld,  a.row_len, a.R,          a.k,          a.col_blocks,
              a.nb,     a.block_size, a.out, a.force_path, dev.err_word};
@@ -656,13 +688,13 @@ cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t s
   // costs: measured at 64 rows, k = 2048, the pair is ~2 us slower at 65536
   // columns, even at 98304 and ~2 us faster at 131072.
   const bool pair = 2 * a.R <= dev.sm_count && a.ld > 98304;
-  cudaError_t e = cudaFuncSetAttribute(pair ? topk_kernel<2> : topk_kernel<1>,
+  cudaError_t e = cudaFuncSetAttribute(pair ? topk_kernel<2, T> : topk_kernel<1, T>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (!pair) {
     const int grid = a.R < dev.sm_count ? a.R : dev.sm_count;
-    topk_kernel<1><<<grid, kT, smem, stream>>>(p);
+    topk_kernel<1, T><<<grid, kT, smem, stream>>>(p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -677,8 +709,15 @@ cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t s
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, topk_kernel<2>, p);
+  e = cudaLaunchKernelEx(&cfg, topk_kernel<2, T>, p);
   return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  if (a.R == 0) return cudaSuccess;
+  return a.bf16 ? launch_topk_t<uint16_t>(a, dev, stream) : launch_topk_t<float>(a, dev, stream);
 }
 
 }  // namespace dsa

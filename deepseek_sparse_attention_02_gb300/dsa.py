@@ -49,6 +49,9 @@ _SIGS = {
     "dsa_candidate_expand": ([_P, _I, _I, _I, _P, _I, _P, _P, _P, _SZ, _P], _I),
     "dsa_candidate_logits": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _I, _I, _P, _I, _I,
                               _P, _P, _SZ, _P, _I64, _P], _I),
+    "dsa_topk_bf16": ([_P, _I64, _P, _I, _I, _P, _I, _I, _P, _I, _P], _I),
+    "dsa_candidate_logits_bf16": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _I, _I, _P, _I,
+                                   _I, _P, _P, _SZ, _P, _I64, _P], _I),
     "dsa_layer_sources": ([_P, _I, _I, _P], _I),
     "dsa_decode_layers_workspace_size": ([_I, _I64, _I], _SZ),
     "dsa_decode_layers": ([_P, _I, _P, _I, _I64, _I64, _I64, _I, _P, _I64, _P, _P, _I, _I, _I, _F,
@@ -129,6 +132,12 @@ def dsa_topk(logits, ld, row_len, R, k, out_idx, col_blocks=None, nb=0, block_si
              force_path=0, stream=None):
     _check(_lib.dsa_topk(_ptr(logits), ld, _ptr(row_len), R, k, _ptr(col_blocks), nb, block_size,
                          _ptr(out_idx), force_path, _stream(stream)))
+
+
+def dsa_topk_bf16(logits, ld, row_len, R, k, out_idx, col_blocks=None, nb=0, block_size=0,
+                  force_path=0, stream=None):
+    _check(_lib.dsa_topk_bf16(_ptr(logits), ld, _ptr(row_len), R, k, _ptr(col_blocks), nb,
+                              block_size, _ptr(out_idx), force_path, _stream(stream)))
 
 
 def dsa_sparse_mla_workspace_size(R: int, k: int) -> int:
@@ -222,3 +231,16 @@ def dsa_decode_layers(layers, keep_indexer, mli, k_page_stride, s_page_stride, k
                                   _ptr(block_table), bt_stride, _ptr(ctx_len), _ptr(row_len),
                                   num_req, next_n, k, float(sm_scale), ld, _ptr(workspace),
                                   workspace_bytes, _stream(stream), side))
+
+
+def dsa_candidate_logits_bf16(q_fp8, q_scale, weights, k_fp4, k_page_stride, k_sf,
+                              sf_page_stride, num_pages, block_table, num_req, next_n,
+                              sparse_indices, nb, block_size, end, schedule, schedule_bytes,
+                              logits, ld, stream=None):
+    bt_stride = block_table.shape[1]
+    _check(_lib.dsa_candidate_logits_bf16(_ptr(q_fp8), _ptr(q_scale), _ptr(weights), _ptr(k_fp4),
+                                          k_page_stride, _ptr(k_sf), sf_page_stride, num_pages,
+                                          _ptr(block_table), bt_stride, num_req, next_n,
+                                          _ptr(sparse_indices), nb, block_size, _ptr(end),
+                                          _ptr(schedule), schedule_bytes, _ptr(logits), ld,
+                                          _stream(stream)))

@@ -15,6 +15,7 @@
  *   a. candidate expansion, once per step                   dsa_candidate_expand
  *   b. candidate (sparse MQA) logits over MXFP4 keys        dsa_candidate_logits
  *   c. top-k over the candidate columns, mapped to tokens   dsa_topk (col_blocks)
+ *   (b and c also with bf16 logits:  dsa_candidate_logits_bf16, dsa_topk_bf16)
  *
  * and a multi-layer decode step with the IndexCache / Multi-layer Indexer
  * selection schedules (JEV Paper Radar efficiency digest) dsa_decode_layers
@@ -151,6 +152,15 @@ dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int
                     const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
                     int force_path, void* stream);
 
+/* dsa_topk over bf16 scores (the vLLM sparse_indexer page's pairing: bf16
+ * sparse logits selected by a bf16 top-k).  Same arguments and result; each
+ * score is widened to f32 exactly, so the selected set is the f32 one of the
+ * same values (bf16 rounding makes ties frequent; they go to the lower
+ * column).  logits: device [R, ld] bf16, ld % 4 == 0, 16-byte aligned. */
+dsa_status dsa_topk_bf16(const uint16_t* logits, int64_t ld, const int32_t* row_len, int R, int k,
+                         const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
+                         int force_path, void* stream);
+
 /* ------------------------------------------------------------------------
  * dsa_sparse_mla_decode -- sparse MLA attention, Eq. (2):
  *
@@ -222,17 +232,25 @@ dsa_status dsa_sparse_mla_decode_static(const uint16_t* q, const uint16_t* kv_ca
  * consumer indexer layers (vLLM sparse_indexer: sparse_indices, end and the
  * kernel schedule are filled by the first consumer layer and reused).
  *
- *   cand           device [R, nb] int32 candidate block ids published by the
- *                  source layer (distinct; ids >= ceil(L/bs) mark padding).
- *   sparse_indices device [R, nb] int32 out: the ids sorted ascending.
+ *   cand           device [R, nb] int32 candidate block ids (blocks of
+ *                  block_size tokens) published by the source layer
+ *                  (distinct; ids >= ceil(L/block_size) mark padding).
+ *   block_size     candidate_block_size: m * 64 tokens, 1 <= m <= 64.  The
+ *                  sparse blocks are 64-token pages (sparse_block_kv = 64): a
+ *                  candidate block b is the m sparse blocks b*m .. b*m+m-1, so
+ *                  a row has ns = nb * m sparse blocks (the page's
+ *                  num_sparse_blocks = candidate_topk_blocks *
+ *                  (candidate_block_size // sparse_block_kv)); ns <= 4096.
+ *   sparse_indices device [R, ns] int32 out: the sparse block ids sorted
+ *                  ascending.
  *   end            device [R] int32 out: valid sparse columns of the row, i.e.
- *                  #{c < nb*bs : 0 <= tok(c) < L_r}, tok(c) =
- *                  sparse_indices[r, c/bs]*bs + c%bs.  (Sorted ascending, the
+ *                  #{c < ns*64 : 0 <= tok(c) < L_r}, tok(c) =
+ *                  sparse_indices[r, c/64]*64 + c%64.  (Sorted ascending, the
  *                  valid columns are a prefix.)
  *   schedule       device, dsa_candidate_schedule_size(R) bytes out: the work
  *                  schedule dsa_candidate_logits reads.
- *   block_size     candidate_block_size; must equal the 64-token page.
- *   nb <= 4096.
+ * The later calls take nb = ns and block_size = 64 (dsa_candidate_logits and
+ * dsa_topk's col_blocks).
  * ---------------------------------------------------------------------- */
 size_t dsa_candidate_schedule_size(int R);
 
@@ -265,6 +283,19 @@ dsa_status dsa_candidate_logits(const uint8_t* q_fp8, const float* q_scale, cons
                                 int next_n, const int32_t* sparse_indices, int nb,
                                 int block_size, const int32_t* end, const void* schedule,
                                 size_t schedule_bytes, float* logits, int64_t ld, void* stream);
+
+/* dsa_candidate_logits writing bf16 logits (each the f32 result rounded to
+ * nearest even), as the vLLM sparse_indexer page's kernels do: half the bytes
+ * written here and read by dsa_topk_bf16.  logits: device [R, ld] bf16. */
+dsa_status dsa_candidate_logits_bf16(const uint8_t* q_fp8, const float* q_scale,
+                                     const float* weights, const uint8_t* k_fp4,
+                                     int64_t k_page_stride, const uint8_t* k_sf,
+                                     int64_t sf_page_stride, int num_pages,
+                                     const int32_t* block_table, int64_t bt_stride, int num_req,
+                                     int next_n, const int32_t* sparse_indices, int nb,
+                                     int block_size, const int32_t* end, const void* schedule,
+                                     size_t schedule_bytes, uint16_t* logits, int64_t ld,
+                                     void* stream);
 
 /* ------------------------------------------------------------------------
  * dsa_decode_layers -- one decode step over several DSA layers with the

@@ -105,3 +105,39 @@ def test_topk_many_rows_one_cta_per_row():
     logits = torch.randn(R, ld, generator=g, device="cuda")
     sel = gpu_topk(logits, ld, L, 2048)
     sets_equal(sel, logits, L, 2048)
+
+
+@pytest.mark.parametrize("force", [0, 1, 2])
+def test_topk_bf16_rows(force):
+    """bf16 scores (many exact ties after rounding): the set equals the
+    oracle's full sort of the same values, ties to the lower column; long rows
+    take the two-CTA kernel, short ones the one-CTA kernel."""
+    from deepseek_sparse_attention_02_gb300 import dsa
+    g = torch.Generator(device="cuda").manual_seed(7)
+    L = torch.tensor([0, 5, 2048, 2049, 9000, 40961, 70001, 131072], dtype=torch.int32,
+                     device="cuda")
+    ld = 131072
+    logits = torch.randn(len(L), ld, generator=g, device="cuda").to(torch.bfloat16)
+    logits[3, 100:2000] = 0.0
+    logits[3, 2000:2049:2] = -0.0
+    out = torch.full((len(L), 2048), -7, dtype=torch.int32, device="cuda")
+    dsa.dsa_topk_bf16(logits, ld, L, len(L), 2048, out, force_path=force)
+    torch.cuda.synchronize()
+    ref = oracle.topk(np_(logits.float()).astype(np.float64), np_(L), 2048)
+    for i in range(len(L)):
+        assert sorted(np_(out)[i].tolist()) == sorted(ref[i].tolist()), f"row {i}"
+
+
+def test_topk_bf16_matches_f32_of_same_values():
+    """A bf16 row and the f32 row of the same (widened) values select the same set."""
+    from deepseek_sparse_attention_02_gb300 import dsa
+    g = torch.Generator(device="cuda").manual_seed(8)
+    R, ld, k = 64, 32768, 2048
+    L = torch.full((R,), ld, dtype=torch.int32, device="cuda")
+    b = (torch.randn(R, ld, generator=g, device="cuda") * 3).to(torch.bfloat16)
+    o16 = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    o32 = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    dsa.dsa_topk_bf16(b, ld, L, R, k, o16)
+    dsa.dsa_topk(b.float().contiguous(), ld, L, R, k, o32)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.sort(o16, dim=1).values, torch.sort(o32, dim=1).values)
