@@ -172,11 +172,12 @@ def build_candidate(device, seed=3):
               si=torch.empty_like(cand), end=torch.empty(R, dtype=torch.int32, device=device),
               sched=torch.zeros(nbytes // 4, dtype=torch.int32, device=device),
               logits=torch.empty((R, nb * 64), device=device),
+              logits16=torch.empty((R, nb * 64), dtype=torch.bfloat16, device=device),
               idx=torch.empty((4, R, TOPK), dtype=torch.int32, device=device))
     return st
 
 
-def candidate_kernels(st):
+def candidate_kernels(st, bf16=False):
     from deepseek_sparse_attention_02_gb300 import dsa
     from deepseek_sparse_attention_02_gb300 import workloads as W
     R, nb = st["R"], st["nb"]
@@ -185,18 +186,19 @@ def candidate_kernels(st):
     ks = [("expand", lambda: dsa.dsa_candidate_expand(st["cand"], R, nb, 64, lay0.ctx_len, 1,
                                                       st["si"], st["end"], st["sched"],
                                                       st["sched_bytes"]))]
+    cl = dsa.dsa_candidate_logits_bf16 if bf16 else dsa.dsa_candidate_logits
+    tk = dsa.dsa_topk_bf16 if bf16 else dsa.dsa_topk
+    buf = st["logits16"] if bf16 else st["logits"]
     for i, case in enumerate(st["layers"]):
         def logits(case=case):
             c = case.cache
-            dsa.dsa_candidate_logits(case.q, case.q_scale, case.w, c, W.FP4_PAGE_BYTES,
-                                     c.data_ptr() + W.FP4_KEY_BYTES, W.FP4_PAGE_BYTES,
-                                     case.layout.num_pages, case.layout.block_table, R, 1,
-                                     st["si"], nb, 64, st["end"], st["sched"], st["sched_bytes"],
-                                     st["logits"], ld)
+            cl(case.q, case.q_scale, case.w, c, W.FP4_PAGE_BYTES, c.data_ptr() + W.FP4_KEY_BYTES,
+               W.FP4_PAGE_BYTES, case.layout.num_pages, case.layout.block_table, R, 1, st["si"],
+               nb, 64, st["end"], st["sched"], st["sched_bytes"], buf, ld)
 
         def topk(i=i):
-            dsa.dsa_topk(st["logits"], ld, st["end"], R, TOPK, st["idx"][i], col_blocks=st["si"],
-                         nb=nb, block_size=64)
+            tk(buf, ld, st["end"], R, TOPK, st["idx"][i], col_blocks=st["si"], nb=nb,
+               block_size=64)
         ks.append((f"cand_logits_{i}", logits))
         ks.append((f"cand_topk_{i}", topk))
     return ks
@@ -405,6 +407,7 @@ def run_ours(args):
     kernels = decode_kernels(st)
     cst = None if args.no_candidate else build_candidate(device)
     ckernels = [] if cst is None else candidate_kernels(cst)
+    ckernels16 = [] if cst is None else candidate_kernels(cst, bf16=True)
     lst = None if args.no_layers else build_layers(st)
     torch.cuda.synchronize()
 
@@ -413,6 +416,7 @@ def run_ours(args):
         total_ms, per = time_kernels(kernels, args.steps, args.warmup, stream)
         if ckernels:
             c_total_ms, c_per = time_kernels(ckernels, args.steps, args.warmup, stream)
+            c16_total_ms, c16_per = time_kernels(ckernels16, args.steps, args.warmup, stream)
         if lst is not None:
             lay_ms, lay_launches = time_layers(st, lst, args.steps, args.warmup, stream)
     barrier(pg, device)
@@ -450,7 +454,11 @@ def run_ours(args):
                 "breakdown_ms": {k: round(v, 4) for k, v in c_per.items()},
                 "candidate_keys_per_s": cand_keys / (c_ms * 1e-3),
                 "logits_hbm_gbs": c_bytes / (c_log * 1e-3) / 1e9,
-                "topk_rows_per_s": cst["R"] / (ctk * 1e-3)}
+                "topk_rows_per_s": cst["R"] / (ctk * 1e-3),
+                "bf16_logits": {
+                    "ms_per_step": c16_total_ms / args.steps,
+                    "breakdown_ms": {k: round(v, 4) for k, v in c16_per.items()},
+                    "candidate_keys_per_s": cand_keys / (c16_total_ms / args.steps * 1e-3)}}
 
     layers = None
     if lst is not None:
@@ -498,7 +506,7 @@ def run_ours(args):
                      "peak_source": peak_src,
                      "alg_bytes_per_launch": alg_bytes},
         "gpu_launches": args.steps * (len(kernels) + (1 if st["wsb"] > 0 else 0)) +
-                        (args.steps * (len(ckernels) + 1) if ckernels else 0) +
+                        (args.steps * (len(ckernels) + 1) if ckernels else 0) * 2 +
                         (lay_launches if lst is not None else 0),
         "e2e": {"value": world * keys_per_step / (e2e_ms * 1e-3), "unit": "keys/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
