@@ -277,3 +277,34 @@ def layer_sources(keep, mli):
         if kept:
             latest = layer
     return out
+
+
+def prefill_chunk_plan(q_lens, ctx_lens, budget_bytes, min_cols=0):
+    """Splits a batch of prefill queries into chunks whose f32 logits scratch
+    [rows, ld] fits budget_bytes, as the vLLM ``sparse_indexer`` builder's
+    prefill chunker does ("budgets fp32 [rows, seq_len]"; ``min_split_seq_len``
+    makes it "size chunks as if every row were this wide").
+
+    Readings: the rows are taken in order (request by request, position by
+    position); a row of request b needs a logits row of max(ctx_lens[b],
+    min_cols) columns, rounded up to a multiple of 4; a chunk's scratch is
+    rows x (its widest row) x 4 bytes; rows are added to the current chunk
+    while that stays within the budget, and a row that alone exceeds it is a
+    chunk by itself.  Returns pieces (chunk, request, row_begin, row_end):
+    each chunk is a run of consecutive pieces, each piece a run of one
+    request's rows."""
+    pieces = []
+    chunk, rows, width = 0, 0, 0
+    for b, (n, c) in enumerate(zip(q_lens, ctx_lens)):
+        w = (max(int(c), int(min_cols)) + 3) // 4 * 4
+        for j in range(int(n)):
+            if rows > 0 and (rows + 1) * max(width, w) * 4 > budget_bytes:
+                chunk += 1
+                rows, width = 0, 0
+            if pieces and pieces[-1][0] == chunk and pieces[-1][1] == b:
+                pieces[-1][3] = j + 1
+            else:
+                pieces.append([chunk, b, j, j + 1])
+            rows += 1
+            width = max(width, w)
+    return [tuple(p) for p in pieces]

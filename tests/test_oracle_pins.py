@@ -507,3 +507,54 @@ def test_layer_sources_invariants():
                     assert j < layer                       # never its own (MLI)
     with pytest.raises(ValueError):
         oracle.layer_sources([0, 1, 1], False)
+
+
+# ---------------------------------------------------- prefill chunk plan --
+def read_plans(golden_dir):
+    out = []
+    with open(os.path.join(golden_dir, "prefill_chunks.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kind, *kv = line.split()
+            d = dict(x.split("=") for x in kv)
+            out.append(([int(x) for x in d["q"].split(",")], [int(x) for x in d["ctx"].split(",")],
+                        int(d["budget"]), int(d["min"]),
+                        [tuple(int(y) for y in x.split(":")) for x in d["pieces"].split(",")]))
+    return out
+
+
+def test_prefill_chunk_plan_hand_worked(golden_dir):
+    plans = read_plans(golden_dir)
+    assert len(plans) == 5
+    for q, ctx, budget, mn, pieces in plans:
+        assert oracle.prefill_chunk_plan(q, ctx, budget, mn) == pieces, (q, ctx, budget, mn)
+
+
+def test_prefill_chunk_plan_invariants():
+    rng = np.random.default_rng(31)
+    for _ in range(300):
+        nreq = int(rng.integers(1, 8))
+        q = rng.integers(0, 40, nreq)
+        ctx = rng.integers(1, 5000, nreq)
+        mn = int(rng.choice([0, 64, 2048]))
+        budget = int(rng.integers(16, 200000))
+        pieces = oracle.prefill_chunk_plan(q, ctx, budget, mn)
+        width = [(max(int(c), mn) + 3) // 4 * 4 for c in ctx]
+        # every row exactly once, in order
+        rows = [(b, j) for c, b, j0, j1 in pieces for j in range(j0, j1)]
+        assert rows == [(b, j) for b in range(nreq) for j in range(int(q[b]))]
+        chunks = sorted({p[0] for p in pieces})
+        assert chunks == list(range(len(chunks)))
+        for ch in chunks:
+            ps = [p for p in pieces if p[0] == ch]
+            n = sum(p[3] - p[2] for p in ps)
+            w = max(width[p[1]] for p in ps)
+            # within budget unless it is a single row
+            assert n * w * 4 <= budget or n == 1
+            # maximal: the next row would not have fit
+            nxt = [p for p in pieces if p[0] == ch + 1]
+            if nxt:
+                w2 = max(w, width[nxt[0][1]])
+                assert (n + 1) * w2 * 4 > budget
