@@ -131,6 +131,52 @@ dsa_status cuda_status(cudaError_t e, const char* what) {
   return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// dsa_indexer_logits / _varlen: the checks and the launch.  Without cu_rows
+// every request has next_n rows; with it, entry i's rows are
+// [cu_rows[i], cu_rows[i+1]) (at most next_n of them, total_rows in all) and
+// it reads block-table row bt_rows[i] (or i).
+dsa_status indexer_impl(const char* fn, const uint8_t* q_fp8, const float* q_scale,
+                        const float* weights, const uint8_t* k_cache, int64_t k_page_stride,
+                        const uint8_t* k_scale, int64_t s_page_stride, int num_pages,
+                        const int32_t* block_table, int64_t bt_stride, const int32_t* ctx_len,
+                        int num_req, int next_n, const int32_t* cu_rows, const int32_t* bt_rows,
+                        int bt_num_rows, int total_rows, float* logits, int64_t ld,
+                        void* stream) {
+  if (!q_fp8 || !q_scale || !weights || !k_cache || !k_scale || !block_table || !ctx_len ||
+      !logits)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (num_req < 0 || next_n < 1 || next_n > 65536 || num_pages < 1 || bt_stride < 1 || ld < 4)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: bad sizes (num_req=%d next_n=%d num_pages=%d bt_stride=%lld ld=%lld)", fn,
+                num_req, next_n, num_pages, (long long)bt_stride, (long long)ld);
+  const int64_t rows = cu_rows ? total_rows : static_cast<int64_t>(num_req) * next_n;
+  if (rows * 64 > (1ll << 31) - 1) return fail(DSA_ERR_UNSUPPORTED, "%s: too many query rows", fn);
+  if (num_req > 4096) return fail(DSA_ERR_UNSUPPORTED, "%s: num_req > 4096", fn);
+  if (k_page_stride < 64 * 128 || k_page_stride % 16 || s_page_stride < 256 ||
+      s_page_stride % 16)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: page strides must cover the page payload and be multiples of 16 bytes", fn);
+  if (!aligned16(k_cache) || !aligned16(k_scale) || !aligned16(q_fp8) || !aligned16(logits) ||
+      ld % 4)
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: k_cache, k_scale, q_fp8 and logits must be 16-byte aligned, ld %% 4 == 0", fn);
+  if (num_req == 0 || rows == 0) return ok();
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  IndexerArgs a{q_fp8,     q_scale,     weights,   k_cache, k_page_stride, k_scale, s_page_stride,
+                num_pages, block_table, bt_stride, ctx_len, num_req,       next_n,  logits,
+                ld};
+  a.cu_rows = cu_rows;
+  a.bt_rows = bt_rows;
+  a.total_rows = static_cast<int>(rows);
+  a.bt_num_rows = bt_num_rows;
+  char msg[256] = "";
+  cudaError_t e = launch_indexer(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
+  if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
+  return cuda_status(e, fn);
+}
+
 // dsa_topk / dsa_topk_bf16: the checks and the launch, for f32 or bf16 scores.
 dsa_status topk_impl(const char* fn, const void* logits, bool bf16, int64_t ld,
                      const int32_t* row_len, int R, int k, const int32_t* col_blocks, int nb,
@@ -237,36 +283,32 @@ dsa_status dsa_indexer_logits(const uint8_t* q_fp8, const float* q_scale, const 
                               const int32_t* block_table, int64_t bt_stride,
                               const int32_t* ctx_len, int num_req, int next_n, float* logits,
                               int64_t ld, void* stream) {
-  const char* fn = "dsa_indexer_logits";
-  if (!q_fp8 || !q_scale || !weights || !k_cache || !k_scale || !block_table || !ctx_len ||
-      !logits)
-    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
-  if (num_req < 0 || next_n < 1 || next_n > 65536 || num_pages < 1 || bt_stride < 1 || ld < 4)
+  return dsa::indexer_impl("dsa_indexer_logits", q_fp8, q_scale, weights, k_cache, k_page_stride,
+                           k_scale, s_page_stride, num_pages, block_table, bt_stride, ctx_len,
+                           num_req, next_n, nullptr, nullptr, 0, 0, logits, ld, stream);
+}
+
+dsa_status dsa_indexer_logits_varlen(const uint8_t* q_fp8, const float* q_scale,
+                                     const float* weights, const uint8_t* k_cache,
+                                     int64_t k_page_stride, const uint8_t* k_scale,
+                                     int64_t s_page_stride, int num_pages,
+                                     const int32_t* block_table, int64_t bt_stride,
+                                     int bt_num_rows, const int32_t* bt_rows,
+                                     const int32_t* ctx_len, const int32_t* cu_rows,
+                                     int num_entries, int max_rows, int total_rows,
+                                     float* logits, int64_t ld, void* stream) {
+  const char* fn = "dsa_indexer_logits_varlen";
+  if (!cu_rows) return fail(DSA_ERR_INVALID_ARG, "%s: cu_rows is NULL", fn);
+  if (max_rows < 1 || max_rows > 65536 || total_rows < 0 || bt_num_rows < 1 ||
+      (!bt_rows && bt_num_rows < num_entries))
     return fail(DSA_ERR_INVALID_ARG,
-                "%s: bad sizes (num_req=%d next_n=%d num_pages=%d bt_stride=%lld ld=%lld)", fn,
-                num_req, next_n, num_pages, (long long)bt_stride, (long long)ld);
-  if (static_cast<int64_t>(num_req) * next_n * 64 > (1ll << 31) - 1)
-    return fail(DSA_ERR_UNSUPPORTED, "%s: too many query rows", fn);
-  if (num_req > 4096) return fail(DSA_ERR_UNSUPPORTED, "%s: num_req > 4096", fn);
-  if (k_page_stride < 64 * 128 || k_page_stride % 16 || s_page_stride < 256 ||
-      s_page_stride % 16)
-    return fail(DSA_ERR_INVALID_ARG,
-                "%s: page strides must cover the page payload and be multiples of 16 bytes", fn);
-  if (!aligned16(k_cache) || !aligned16(k_scale) || !aligned16(q_fp8) || !aligned16(logits) ||
-      ld % 4)
-    return fail(DSA_ERR_INVALID_ARG,
-                "%s: k_cache, k_scale, q_fp8 and logits must be 16-byte aligned, ld %% 4 == 0", fn);
-  if (num_req == 0) return ok();
-  DeviceInfo dev;
-  dsa_status st = device_ready(&dev);
-  if (st != DSA_OK) return st;
-  IndexerArgs a{q_fp8,     q_scale,     weights,   k_cache, k_page_stride, k_scale, s_page_stride,
-                num_pages, block_table, bt_stride, ctx_len, num_req,       next_n,  logits,
-                ld};
-  char msg[256] = "";
-  cudaError_t e = launch_indexer(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
-  if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
-  return cuda_status(e, fn);
+                "%s: need 1 <= max_rows <= 65536, total_rows >= 0, bt_num_rows >= 1 (and >= "
+                "num_entries without bt_rows)",
+                fn);
+  return dsa::indexer_impl(fn, q_fp8, q_scale, weights, k_cache, k_page_stride, k_scale,
+                           s_page_stride, num_pages, block_table, bt_stride, ctx_len, num_entries,
+                           max_rows, cu_rows, bt_rows, bt_num_rows, total_rows, logits, ld,
+                           stream);
 }
 
 dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
@@ -384,6 +426,44 @@ dsa_status dsa_candidate_logits_bf16(const uint8_t* q_fp8, const float* q_scale,
                                k_page_stride, k_sf, sf_page_stride, num_pages, block_table,
                                bt_stride, num_req, next_n, sparse_indices, nb, block_size, end,
                                schedule, schedule_bytes, nullptr, logits, ld, stream);
+}
+
+dsa_status dsa_sparse_mla_decode_varlen(const uint16_t* q, const uint16_t* kv_cache,
+                                        int64_t kv_page_stride, int num_pages,
+                                        const int32_t* block_table, int64_t bt_stride,
+                                        int bt_num_rows, const int32_t* row_bt, int R,
+                                        const int32_t* idx, int k, float sm_scale, uint16_t* out,
+                                        float* lse, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  const char* fn = "dsa_sparse_mla_decode_varlen";
+  if (!q || !kv_cache || !block_table || !row_bt || !idx || !out)
+    return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+  if (R < 0 || bt_num_rows < 1 || num_pages < 1 || bt_stride < 1 || k < 1 ||
+      k > DSA_MAX_TOPK || !(sm_scale > 0.f))
+    return fail(DSA_ERR_INVALID_ARG, "%s: bad sizes or scale", fn);
+  if (kv_page_stride != 64 * 576 * 2 || !aligned16(kv_cache) || !aligned16(q) ||
+      !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG,
+                "%s: latent pages must be contiguous (kv_page_stride == 73728); q, kv and out "
+                "16-byte aligned",
+                fn);
+  if (static_cast<int64_t>(num_pages) * 64 > (1ll << 31) - 1)
+    return fail(DSA_ERR_UNSUPPORTED, "%s: more than 2^31 cached latent rows", fn);
+  if (R > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
+  if (R == 0) return ok();
+  const size_t need = mla_workspace_size(R, k);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace_bytes);
+  DeviceInfo dev;
+  dsa_status st = device_ready(&dev);
+  if (st != DSA_OK) return st;
+  MlaArgs a{q,   kv_cache, kv_page_stride, num_pages, block_table, bt_stride, 1,         1,
+            idx, k,        sm_scale,       out,       lse,         workspace, workspace_bytes};
+  a.row_bt = row_bt;
+  a.bt_num_rows = bt_num_rows;
+  a.rows = R;
+  return cuda_status(launch_sparse_mla(a, dev, static_cast<cudaStream_t>(stream)), fn);
 }
 
 size_t dsa_sparse_mla_static_scratch_bytes(void) { return mla_static_scratch_bytes(); }

@@ -66,13 +66,28 @@ struct KParams {
   int64_t bt_stride;
   const int32_t* ctx_len;
   int num_req;
-  int next_n;
+  int next_n;               // rows per request, or (with cu_rows) at most this many
+  const int32_t* cu_rows;   // null, or [num_req + 1]: request i's rows are [cu_rows[i], cu_rows[i+1])
+  const int32_t* bt_rows;   // null, or [num_req]: the block-table row of request i
+  int total_rows;           // with cu_rows: the rows of q and logits
+  int bt_num_rows;          // with bt_rows: the rows of the block table
   float* logits;
   int64_t ld;
   uint32_t* err;
 };
 
 __device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
+
+// Rows of request i: next_n, or (varlen) cu_rows[i+1] - cu_rows[i]; a range
+// outside [0, total_rows] is treated as empty (and reported by the caller).
+__device__ __forceinline__ int rows_of(const int32_t* cu, int next_n, int total, int i) {
+  if (!cu) return next_n;
+  const int a = cu[i], b = cu[i + 1];
+  return (a < 0 || b < a || b > total) ? 0 : b - a;
+}
+__device__ __forceinline__ bool bad_rows(const int32_t* cu, int total, int i) {
+  return cu && (cu[i] < 0 || cu[i + 1] < cu[i] || cu[i + 1] > total);
+}
 
 __device__ __forceinline__ int group_tiles(int ctx, int next_n, int G, int gsub) {
   const int jlast = min(gsub * G + G, next_n) - 1;
@@ -86,13 +101,21 @@ __device__ __forceinline__ int group_tiles(int ctx, int next_n, int G, int gsub)
 struct Cursor {
   const int* prefix;  // smem [num_req + 1] exclusive chunk prefix per request
   const int32_t* ctx_len;
-  int num_req, next_n, G, ngroups;
+  const int32_t* cu_rows;  // null: every request has next_n rows
+  int num_req, next_n, G, total_rows;
   int c, c_end;
   int req, gsub, ctx, tiles, gchunk, nchunk;
+  int nn, ngroups, rbase;  // the current request's rows, row groups, first row
   int gcount;  // groups entered so far (the current group's Q slot is gcount & 1)
 
+  __device__ void enter_request() {
+    ctx = ctx_len[req];
+    nn = rows_of(cu_rows, next_n, total_rows, req);
+    rbase = cu_rows ? cu_rows[req] : req * next_n;
+    ngroups = div_up(nn, G);
+  }
   __device__ void enter_group() {
-    tiles = group_tiles(ctx, next_n, G, gsub);
+    tiles = group_tiles(ctx, nn, G, gsub);
     nchunk = div_up(tiles, kChunkTiles);
   }
   // Moves to the first group with chunks at or after (req, gsub).
@@ -102,7 +125,7 @@ struct Cursor {
       if (gsub >= ngroups || prefix[req + 1] == prefix[req]) {
         ++req;
         gsub = 0;
-        if (req < num_req) ctx = ctx_len[req];
+        if (req < num_req) enter_request();
         continue;
       }
       enter_group();
@@ -110,14 +133,15 @@ struct Cursor {
       ++gsub;
     }
   }
-  __device__ void init(const int* pre, const int32_t* ctxs, int nreq, int nn, int g, int c0,
-                       int c1) {
+  __device__ void init(const int* pre, const int32_t* ctxs, const int32_t* cu, int total,
+                       int nreq, int nrows_req, int g, int c0, int c1) {
     prefix = pre;
     ctx_len = ctxs;
+    cu_rows = cu;
+    total_rows = total;
     num_req = nreq;
-    next_n = nn;
+    next_n = nrows_req;
     G = g;
-    ngroups = div_up(nn, g);
     c = c0;
     c_end = c1;
     gcount = 0;
@@ -128,7 +152,7 @@ struct Cursor {
       if (prefix[mid] <= c) lo = mid; else hi = mid;
     }
     req = lo;
-    ctx = ctx_len[req];
+    enter_request();
     int rem = c - prefix[req];
     gsub = 0;
     for (;;) {
@@ -142,8 +166,8 @@ struct Cursor {
   __device__ bool valid() const { return c < c_end; }
   __device__ int tile_begin() const { return gchunk * kChunkTiles; }
   __device__ int tile_end() const { return min(tiles, gchunk * kChunkTiles + kChunkTiles); }
-  __device__ int row0() const { return req * next_n + gsub * G; }
-  __device__ int nrows() const { return min(G, next_n - gsub * G); }
+  __device__ int row0() const { return rbase + gsub * G; }
+  __device__ int nrows() const { return min(G, nn - gsub * G); }
   // Advances to the next chunk; returns true if it leaves the current group.
   __device__ bool next() {
     ++c;
@@ -158,7 +182,7 @@ struct Cursor {
   // Row length of row j of the current group.
   __device__ int row_len(int j) const {
     const int jj = gsub * G + j;
-    return max(0, ctx - (next_n - 1 - jj));
+    return max(0, ctx - (nn - 1 - jj));
   }
 };
 
@@ -199,11 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
 
   // ---- per-request chunk counts and their exclusive prefix (all threads) ----
-  const int ngroups = div_up(p.next_n, G);
   for (int i = tid; i < p.num_req; i += kThreads) {
     const int ctx = p.ctx_len[i];
+    const int nn = rows_of(p.cu_rows, p.next_n, p.total_rows, i);
+    if (bad_rows(p.cu_rows, p.total_rows, i)) raise_error(p.err, kErrBadIndex);
+    const int ngroups = nn > 0 ? div_up(nn, G) : 0;
     int n = 0;
-    for (int g = 0; g < ngroups; ++g) n += div_up(group_tiles(ctx, p.next_n, G, g), kChunkTiles);
+    for (int g = 0; g < ngroups; ++g) n += div_up(group_tiles(ctx, nn, G, g), kChunkTiles);
     s.prefix[i + 1] = n;
   }
   if (tid == 0) {
@@ -278,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers --
     Cursor cur;
-    cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
+    cur.init(s.prefix, p.ctx_len, p.cu_rows, p.total_rows, p.num_req, p.next_n, G, c0, c1);
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       if (warp == 0) tma_prefetch_desc(&tm_q);
@@ -294,7 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int npg = div_up(c.row_len(c.nrows() - 1), 64);
       const int pg = 2 * c.tile_begin() + lane;
       if (lane >= 2 * kChunkTiles || pg >= npg) return -1;
-      return pg < p.bt_stride ? p.bt[static_cast<int64_t>(c.req) * p.bt_stride + pg] : -2;
+      const int64_t btr = p.bt_rows ? p.bt_rows[c.req] : c.req;
+      if (btr < 0 || (p.bt_rows && btr >= p.bt_num_rows)) return -2;  // reported as a bad page
+      return pg < p.bt_stride ? p.bt[btr * p.bt_stride + pg] : -2;
     };
     Cursor ahead = cur;
     int pages_cur = chunk_pages(cur);
@@ -369,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = warp - kMmaWarp;
     if (lane == 0) {
       Cursor cur;
-      cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
+      cur.init(s.prefix, p.ctx_len, p.cu_rows, p.total_rows, p.num_req, p.next_n, G, c0, c1);
       int lt = 0;
       bool new_group = true;
       while (cur.valid() && !*abort) {
@@ -408,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
     const int row_in_tile = quad * 32 + lane;
     Cursor cur;
-    cur.init(s.prefix, p.ctx_len, p.num_req, p.next_n, G, c0, c1);
+    cur.init(s.prefix, p.ctx_len, p.cu_rows, p.total_rows, p.num_req, p.next_n, G, c0, c1);
     int lt = 0;
     while (cur.valid() && !*abort) {
       const int slot = cur.gcount & 1;
@@ -492,6 +520,10 @@ cudaError_t launch_g(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t s
   p.ctx_len = a.ctx_len;
   p.num_req = a.num_req;
   p.next_n = a.next_n;
+  p.cu_rows = a.cu_rows;
+  p.bt_rows = a.bt_rows;
+  p.total_rows = a.total_rows;
+  p.bt_num_rows = a.bt_num_rows;
   p.logits = a.logits;
   p.ld = a.ld;
   p.err = dev.err_word;
@@ -520,7 +552,8 @@ cudaError_t launch_indexer(const IndexerArgs& a, const DeviceInfo& dev, cudaStre
   }
   {
     // q: [R*64 rows][128 bytes]; one box = the N rows of a row group
-    const uint64_t rows = static_cast<uint64_t>(a.num_req) * a.next_n * 64;
+    const uint64_t rows =
+        (a.cu_rows ? static_cast<uint64_t>(a.total_rows) : static_cast<uint64_t>(a.num_req) * a.next_n) * 64;
     const uint64_t dims[2] = {128, rows};
     const uint64_t strides[1] = {128};
     const uint32_t box[2] = {128, static_cast<uint32_t>(64 * G)};

@@ -41,9 +41,13 @@ struct IndexerArgs {
   int64_t bt_stride;
   const int32_t* ctx_len;
   int num_req;
-  int next_n;
+  int next_n;               // rows per request, or (with cu_rows) the largest row count
   float* logits;
   int64_t ld;
+  const int32_t* cu_rows = nullptr;  // varlen: request i's rows [cu_rows[i], cu_rows[i+1])
+  const int32_t* bt_rows = nullptr;  // varlen: block-table row of request i
+  int total_rows = 0;                // varlen: cu_rows[num_req]
+  int bt_num_rows = 0;               // varlen: rows of the block table
 };
 
 cudaError_t launch_indexer(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t stream,
@@ -81,6 +85,9 @@ struct MlaArgs {
   float* lse;
   void* ws;
   size_t ws_bytes;
+  const int32_t* row_bt = nullptr;  // varlen: block-table row of each of the `rows` query rows
+  int bt_num_rows = 0;
+  int rows = 0;
 };
 
 size_t mla_workspace_size(int R, int k);

@@ -62,6 +62,8 @@ struct MParams {
   int64_t bt_stride;
   int num_pages;
   int next_n;
+  const int32_t* row_bt;  // null, or [R]: the block-table row of each query row
+  int bt_num_rows;        // with row_bt: the rows of the block table
   const int32_t* idx;
   int k;
   float scale_log2;
@@ -119,7 +121,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row = blockIdx.x;
   const int vh = blockIdx.y;
   const int split = blockIdx.z;
-  const int req = row / p.next_n;
+  // the block-table row of this query row (an out-of-range one reads nothing)
+  int req = p.row_bt ? p.row_bt[row] : row / p.next_n;
+  if (p.row_bt && (req < 0 || req >= p.bt_num_rows)) {
+    if (threadIdx.x == 0) raise_error(p.err, kErrBadPage);
+    req = -1;
+  }
   const int s0 = split * p.tokens_per_split;
   const int s1 = min(p.k, s0 + p.tokens_per_split);
   const int ntile = s1 > s0 ? (s1 - s0 + kTile - 1) / kTile : 0;
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 4; ++u) {
         const int64_t pg_i = t[u] / 64;
         pg[u] = (t[u] >= 0 && pg_i < p.bt_stride)
-                    ? p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i] : -1;
+                    ? (req >= 0 ? p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i] : -1) : -1;
       }
     };
     auto make_rows = [&](const int (&t)[4], const int (&pg)[4], int (&r)[4]) {
@@ -553,7 +560,7 @@ size_t mla_workspace_size(int R, int k) {
 }
 
 cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  const int R = a.num_req * a.next_n;
+  const int R = a.row_bt ? a.rows : a.num_req * a.next_n;
   const int ns = choose_nsplit(R, a.k);
   const int tiles = (a.k + kTile - 1) / kTile;
   const int tps = ((tiles + ns - 1) / ns) * kTile;
@@ -573,6 +580,8 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   p.bt_stride = a.bt_stride;
   p.num_pages = a.num_pages;
   p.next_n = a.next_n;
+  p.row_bt = a.row_bt;
+  p.bt_num_rows = a.bt_num_rows;
   p.idx = a.idx;
   p.k = a.k;
   p.scale_log2 = a.sm_scale * kLog2e;
@@ -628,7 +637,7 @@ size_t mla_static_scratch_bytes() { return kStaticScratchBytes; }
 
 cudaError_t launch_sparse_mla_static(const MlaArgs& a_in, const DeviceInfo& dev,
                                      cudaStream_t stream, size_t* need) {
-  const int R = a_in.num_req * a_in.next_n;
+  const int R = a_in.row_bt ? a_in.rows : a_in.num_req * a_in.next_n;
   *need = mla_workspace_size(R, a_in.k);
   if (*need > kStaticScratchBytes) return cudaErrorMemoryAllocation;
   MlaArgs a = a_in;

@@ -52,6 +52,12 @@ _SIGS = {
     "dsa_topk_bf16": ([_P, _I64, _P, _I, _I, _P, _I, _I, _P, _I, _P], _I),
     "dsa_candidate_logits_bf16": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _I, _I, _P, _I,
                                    _I, _P, _P, _SZ, _P, _I64, _P], _I),
+    "dsa_prefill_chunk_plan": ([_P, _P, _I, _I64, _I64, _P, _I, _P], _I),
+    "dsa_indexer_logits_varlen": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _I, _P, _P, _P,
+                                   _I, _I, _I, _P, _I64, _P], _I),
+    "dsa_varlen_row_lengths": ([_P, _P, _I, _I, _P, _P], _I),
+    "dsa_sparse_mla_decode_varlen": ([_P, _P, _I64, _I, _P, _I64, _I, _P, _I, _P, _I, _F, _P, _P,
+                                      _P, _SZ, _P], _I),
     "dsa_layer_sources": ([_P, _I, _I, _P], _I),
     "dsa_decode_layers_workspace_size": ([_I, _I64, _I], _SZ),
     "dsa_decode_layers": ([_P, _I, _P, _I, _I64, _I64, _I64, _I, _P, _I64, _P, _P, _I, _I, _I, _F,
@@ -244,3 +250,44 @@ def dsa_candidate_logits_bf16(q_fp8, q_scale, weights, k_fp4, k_page_stride, k_s
                                           _ptr(sparse_indices), nb, block_size, _ptr(end),
                                           _ptr(schedule), schedule_bytes, _ptr(logits), ld,
                                           _stream(stream)))
+
+
+def dsa_prefill_chunk_plan(q_len, ctx_len, budget_bytes: int, min_cols: int = 0) -> list:
+    """Host-only: [(chunk, request, row_begin, row_end), ...]."""
+    n = len(q_len)
+    ql = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in q_len])
+    cl = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in ctx_len])
+    cap = sum(int(x) for x in q_len) + 1
+    out = (ctypes.c_int32 * (4 * cap))()
+    npc = ctypes.c_int(0)
+    _check(_lib.dsa_prefill_chunk_plan(ctypes.cast(ql, _P), ctypes.cast(cl, _P), n, budget_bytes,
+                                       min_cols, ctypes.cast(out, _P), cap, ctypes.byref(npc)))
+    return [tuple(out[4 * i:4 * i + 4]) for i in range(npc.value)]
+
+
+def dsa_indexer_logits_varlen(q_fp8, q_scale, weights, k_cache, k_page_stride, k_scale,
+                              s_page_stride, num_pages, block_table, bt_rows, ctx_len, cu_rows,
+                              num_entries, max_rows, total_rows, logits, ld, stream=None):
+    bt_num_rows, bt_stride = block_table.shape
+    _check(_lib.dsa_indexer_logits_varlen(_ptr(q_fp8), _ptr(q_scale), _ptr(weights),
+                                          _ptr(k_cache), k_page_stride, _ptr(k_scale),
+                                          s_page_stride, num_pages, _ptr(block_table), bt_stride,
+                                          bt_num_rows, _ptr(bt_rows), _ptr(ctx_len),
+                                          _ptr(cu_rows), num_entries, max_rows, total_rows,
+                                          _ptr(logits), ld, _stream(stream)))
+
+
+def dsa_varlen_row_lengths(ctx_len, cu_rows, num_entries, total_rows, row_len, stream=None):
+    _check(_lib.dsa_varlen_row_lengths(_ptr(ctx_len), _ptr(cu_rows), num_entries, total_rows,
+                                       _ptr(row_len), _stream(stream)))
+
+
+def dsa_sparse_mla_decode_varlen(q, kv_cache, kv_page_stride, num_pages, block_table, row_bt, R,
+                                 idx, k, sm_scale, out, lse, workspace, workspace_bytes,
+                                 stream=None):
+    bt_num_rows, bt_stride = block_table.shape
+    _check(_lib.dsa_sparse_mla_decode_varlen(_ptr(q), _ptr(kv_cache), kv_page_stride, num_pages,
+                                             _ptr(block_table), bt_stride, bt_num_rows,
+                                             _ptr(row_bt), R, _ptr(idx), k, float(sm_scale),
+                                             _ptr(out), _ptr(lse), _ptr(workspace),
+                                             workspace_bytes, _stream(stream)))

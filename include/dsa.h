@@ -298,6 +298,69 @@ dsa_status dsa_candidate_logits_bf16(const uint8_t* q_fp8, const float* q_scale,
                                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * Prefill in chunks (the vLLM sparse_indexer page: "the prefill chunker
+ * (which budgets fp32 [rows, seq_len])", chunks of rows with per-row K
+ * ranges that may come from several requests).
+ *
+ * dsa_prefill_chunk_plan (host) -- splits a batch's query rows into chunks.
+ * Rows are taken request by request, position by position; a row of request
+ * b needs a logits row of max(ctx_len[b], min_cols) columns (min_cols is the
+ * page's min_split_seq_len), rounded up to a multiple of 4; a chunk's f32
+ * scratch is rows x (its widest row) x 4 bytes, and rows join the current
+ * chunk while that stays within budget_bytes (a row alone above it is a chunk
+ * by itself).  Writes *num_pieces records pieces[4 i .. 4 i + 3] = (chunk,
+ * request, row_begin, row_end): each chunk is a run of consecutive pieces,
+ * each piece rows [row_begin, row_end) of one request.  q_len, ctx_len: host
+ * [num_req].  DSA_ERR_WORKSPACE if more than max_pieces pieces are needed.
+ *
+ * A chunk is run as entries, one per piece: entry e = (request b, rows
+ * [j0, j1)) has j1 - j0 rows, the last of which sees ctx_len[b] - (q_len[b] -
+ * j1) tokens, and reads block-table row b.
+ *
+ * dsa_indexer_logits_varlen -- dsa_indexer_logits over entries of different
+ * row counts: entry e's rows are [cu_rows[e], cu_rows[e+1]) (device
+ * [num_entries + 1], total_rows = cu_rows[num_entries], every entry at most
+ * max_rows rows), row cu_rows[e] + j of n_e sees ctx_len[e] - (n_e - 1 - j)
+ * tokens of block-table row bt_rows[e] (device [num_entries]; NULL = row e),
+ * and the block table has bt_num_rows rows.  q_fp8 / q_scale / weights /
+ * logits have total_rows rows.  Entries whose row range is reversed or past
+ * total_rows, and block-table rows outside [0, bt_num_rows), are skipped and
+ * set DSA_DEVERR_BAD_INDEX / DSA_DEVERR_BAD_PAGE.
+ *
+ * dsa_varlen_row_lengths -- row_len[cu_rows[e] + j] = that row's token count
+ * (device [total_rows]), the row_len dsa_topk takes.
+ *
+ * dsa_sparse_mla_decode_varlen -- dsa_sparse_mla_decode for R query rows whose
+ * block-table rows are row_bt[r] (device [R]; rows outside [0, bt_num_rows)
+ * read nothing and set DSA_DEVERR_BAD_PAGE); workspace as
+ * dsa_sparse_mla_workspace_size(R, k).
+ * ---------------------------------------------------------------------- */
+dsa_status dsa_prefill_chunk_plan(const int32_t* q_len, const int32_t* ctx_len, int num_req,
+                                  int64_t budget_bytes, int64_t min_cols, int32_t* pieces,
+                                  int max_pieces, int* num_pieces);
+
+dsa_status dsa_indexer_logits_varlen(const uint8_t* q_fp8, const float* q_scale,
+                                     const float* weights, const uint8_t* k_cache,
+                                     int64_t k_page_stride, const uint8_t* k_scale,
+                                     int64_t s_page_stride, int num_pages,
+                                     const int32_t* block_table, int64_t bt_stride,
+                                     int bt_num_rows, const int32_t* bt_rows,
+                                     const int32_t* ctx_len, const int32_t* cu_rows,
+                                     int num_entries, int max_rows, int total_rows,
+                                     float* logits, int64_t ld, void* stream);
+
+dsa_status dsa_varlen_row_lengths(const int32_t* ctx_len, const int32_t* cu_rows, int num_entries,
+                                  int total_rows, int32_t* row_len, void* stream);
+
+dsa_status dsa_sparse_mla_decode_varlen(const uint16_t* q, const uint16_t* kv_cache,
+                                        int64_t kv_page_stride, int num_pages,
+                                        const int32_t* block_table, int64_t bt_stride,
+                                        int bt_num_rows, const int32_t* row_bt, int R,
+                                        const int32_t* idx, int k, float sm_scale, uint16_t* out,
+                                        float* lse, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
+/* ------------------------------------------------------------------------
  * dsa_decode_layers -- one decode step over several DSA layers with the
  * cross-layer selection schedules of the Multi-layer Indexer (MLI) abstract
  * ("JEV Paper Radar" efficiency digest, 2026-11-04):
