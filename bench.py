@@ -260,6 +260,89 @@ def time_layers(st, lst, steps, warmup, stream):
     return res, launches
 
 
+def build_prefill(device, ctx=65536, nq=4096, budget=256 << 20):
+    """The chunked-prefill workload: one request with a 65536-token FP8 key cache
+    and latent cache, its last 4096 positions as query rows (each sees the
+    tokens up to itself), top-2048 and the sparse attention per row; run in the
+    chunks the plan gives for a 256 MiB logits budget, and in one chunk."""
+    import numpy as np
+    import torch
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case = W.make_indexer_case([ctx], next_n=nq, seed=4, device=device)
+    mla = W.make_mla_case(nq, case.layout.num_pages, seed=4, device=device)
+    plans = {}
+    for name, b in (("chunked", budget), ("one_chunk", None)):
+        pieces = dsa.dsa_prefill_chunk_plan([nq], [ctx], b or (nq + 1) * ctx * 4)
+        chunks = []
+        for ch in sorted({p[0] for p in pieces}):
+            ps = [p for p in pieces if p[0] == ch]
+            j0, j1 = ps[0][2], ps[-1][3]
+            n = j1 - j0
+            ld = (ctx + 3) // 4 * 4
+            chunks.append(dict(
+                j0=j0, n=n, ld=ld,
+                cu=torch.tensor([0, n], dtype=torch.int32, device=device),
+                ctx=torch.tensor([ctx - (nq - j1)], dtype=torch.int32, device=device),
+                btr=torch.zeros(1, dtype=torch.int32, device=device),
+                row_bt=torch.zeros(n, dtype=torch.int32, device=device)))
+        nmax = max(c["n"] for c in chunks)
+        wsb = dsa.dsa_sparse_mla_workspace_size(nmax, TOPK)
+        plans[name] = dict(chunks=chunks,
+                           logits=torch.empty((nmax, chunks[0]["ld"]), device=device),
+                           row_len=torch.empty(nmax, dtype=torch.int32, device=device),
+                           sel=torch.empty((nmax, TOPK), dtype=torch.int32, device=device),
+                           ws=torch.empty(max(wsb, 16), dtype=torch.uint8, device=device),
+                           wsb=wsb)
+    out = torch.empty((nq, W.MLA_HEADS, W.MLA_DV), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((nq, W.MLA_HEADS), device=device)
+    return dict(case=case, mla=mla, plans=plans, out=out, lse=lse, nq=nq, ctx=ctx, budget=budget)
+
+
+def prefill_step(pst, plan):
+    """One chunked prefill through the public API; returns the launches made."""
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case, mla = pst["case"], pst["mla"]
+    lay, c = case.layout, case.cache
+    P = pst["plans"][plan]
+    launches = 0
+    for ch in P["chunks"]:
+        j0, n, ld = ch["j0"], ch["n"], ch["ld"]
+        logits = P["logits"][:n]
+        dsa.dsa_indexer_logits_varlen(case.q[j0:j0 + n], case.q_scale[j0:j0 + n],
+                                      case.w[j0:j0 + n], c, W.FP8_PAGE_BYTES,
+                                      c.data_ptr() + W.FP8_KEY_BYTES, W.FP8_PAGE_BYTES,
+                                      lay.num_pages, lay.block_table, ch["btr"], ch["ctx"],
+                                      ch["cu"], 1, n, n, logits, ld)
+        dsa.dsa_varlen_row_lengths(ch["ctx"], ch["cu"], 1, n, P["row_len"])
+        dsa.dsa_topk(logits, ld, P["row_len"], n, TOPK, P["sel"])
+        wsb = dsa.dsa_sparse_mla_workspace_size(n, TOPK)
+        dsa.dsa_sparse_mla_decode_varlen(mla.q[j0:j0 + n], mla.kv, 64 * 576 * 2, lay.num_pages,
+                                         lay.block_table, ch["row_bt"], n, P["sel"][:n], TOPK,
+                                         mla.scale, pst["out"][j0:j0 + n], pst["lse"][j0:j0 + n],
+                                         P["ws"], P["wsb"])
+        launches += 5 + (1 if wsb > 0 else 0)
+    return launches
+
+
+def time_prefill(pst, steps, warmup, stream):
+    import torch
+    res, launches = {}, 0
+    for plan in ("chunked", "one_chunk"):
+        for _ in range(warmup):
+            prefill_step(pst, plan)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            launches += prefill_step(pst, plan)
+        b.record(stream)
+        torch.cuda.synchronize()
+        res[plan] = a.elapsed_time(b) / steps
+    return res, launches
+
+
 def time_kernels(kernels, steps, warmup, stream):
     """Runs `steps` timed passes; returns (total ms, {name: mean ms per launch})."""
     import torch
@@ -409,6 +492,7 @@ def run_ours(args):
     ckernels = [] if cst is None else candidate_kernels(cst)
     ckernels16 = [] if cst is None else candidate_kernels(cst, bf16=True)
     lst = None if args.no_layers else build_layers(st)
+    pst = None if args.no_prefill else build_prefill(device)
     torch.cuda.synchronize()
 
     barrier(pg, device)
@@ -419,6 +503,8 @@ def run_ours(args):
             c16_total_ms, c16_per = time_kernels(ckernels16, args.steps, args.warmup, stream)
         if lst is not None:
             lay_ms, lay_launches = time_layers(st, lst, args.steps, args.warmup, stream)
+        if pst is not None:
+            pre_ms, pre_launches = time_prefill(pst, args.steps, args.warmup, stream)
     barrier(pg, device)
     torch.cuda.synchronize()
     assert dsa.dsa_get_device_error() == 0, "device error word set during the benchmark"
@@ -471,6 +557,20 @@ def run_ours(args):
                   "ms_per_step": {k: round(v, 4) for k, v in lay_ms.items()},
                   "speedup_vs_r1_seq": {k: round(base / v, 3) for k, v in lay_ms.items()}}
 
+    prefill = None
+    if pst is not None:
+        nrows, ctxn = pst["nq"], pst["ctx"]
+        nchunks = len(pst["plans"]["chunked"]["chunks"])
+        pairs = sum(ctxn - (nrows - 1 - j) for j in range(nrows))
+        prefill = {"workload": f"1 request, {ctxn}-token cache, its last {nrows} positions as "
+                               f"query rows: indexer, top-{TOPK}, sparse MLA per row",
+                   "chunked": {"budget_bytes": pst["budget"], "chunks": nchunks,
+                               "ms": round(pre_ms["chunked"], 4),
+                               "keys_per_s": pairs / (pre_ms["chunked"] * 1e-3)},
+                   "one_chunk": {"logits_bytes": nrows * ctxn * 4,
+                                 "ms": round(pre_ms["one_chunk"], 4),
+                                 "keys_per_s": pairs / (pre_ms["one_chunk"] * 1e-3)}}
+
     line = {
         "metric": METRIC,
         "value": value,
@@ -501,13 +601,15 @@ def run_ours(args):
                        "tflops": R * 2 * 128 * TOPK * (576 + 512) / (per["sparse_mla"] * 1e-3) / 1e12},
         "candidate_path": cand,
         "layer_schedules": layers,
+        "prefill_chunks": prefill,
         "roofline": {"kernel": "dsa_indexer_logits", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": peak_src,
                      "alg_bytes_per_launch": alg_bytes},
         "gpu_launches": args.steps * (len(kernels) + (1 if st["wsb"] > 0 else 0)) +
                         (args.steps * (len(ckernels) + 1) if ckernels else 0) * 2 +
-                        (lay_launches if lst is not None else 0),
+                        (lay_launches if lst is not None else 0) +
+                        (pre_launches if pst is not None else 0),
         "e2e": {"value": world * keys_per_step / (e2e_ms * 1e-3), "unit": "keys/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks.summary(),
@@ -564,6 +666,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--requests", type=int, default=32,
                     help="decode requests (32 = the 128K workload; fewer for profiling)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the chunked-prefill measurement")
     ap.add_argument("--no-layers", action="store_true",
                     help="skip the multi-layer IndexCache / MLI schedule measurement")
     ap.add_argument("--no-candidate", action="store_true",
