@@ -3,31 +3,35 @@
 // over only the k selected latents c_s (576 = 512 latent + 64 rope elements;
 // the value is the first 512).
 //
-// Work unit = one CTA per (row, value half vh, split); 128 selected tokens per
-// tile.
-//   warps 0-7  gather: Q of the row once (TMA, nine 128B-swizzled [128 x 64]
-//              K-chunks); then per tile the nine [128 tokens x 64] K-chunks of
-//              the selected latents, and one tile later the four value chunks
-//              of this CTA's half again (an L2 hit), through a 5-slot ring of
-//              16 KB, by 16-byte cp.async (each thread copies 4 pieces of a
-//              chunk; completion is signalled with cp.async.mbarrier.arrive, so
-//              no thread waits for its copies; a skipped selection is
-//              zero-filled);
-//   warps 8-11 softmax (one thread per head / TMEM lane): mask skipped
-//              selections, running max with lazy rescaling of O (only when the
-//              max grows by more than 2^8), P = exp2(S*scale*log2e - m) packed as
-//              bf16 into the TMEM columns of the S tile it came from;
-//   warp 12    tcgen05 issuer of S = Q K^T (kind::f16, M = 128 heads, N = 128
-//              tokens, K = 576) into one of two TMEM tiles;
-//   warp 13    tcgen05 issuer of O[128 x 256] += P V_half with P read from TMEM
-//              and V read MN-major from the ring (N = 256 when the four value
-//              chunks are contiguous in the ring, else two MMAs).  The ring
-//              holds, in order, S(0), S(1), PV(0), S(2), PV(1), ...
-// Many gathering warps matter: scattered 128-byte latent lines reach ~4-5 TB/s
-// this way, about twice the rate of TMA tile::gather4 for the same lines.
-// The 512 value columns are split over two CTAs because O for 128 heads x 512
-// columns in f32 would fill all 512 TMEM columns; each CTA recomputes S.
-// With more than one split the CTAs write unnormalised partial O plus their
+// Work unit = a cluster of two CTAs per (row, split); 128 selected tokens per
+// tile.  The pair divides the work by operand instead of by output columns, so
+// every selected latent crosses into the pair's shared memory once for S and
+// once for P V, and S is computed once:
+//
+//  CTA 0, the score CTA (TMEM: S tile [128 heads x 128 tokens] f32 at columns
+//  0-127, Q of the row at 128-415, lane = head, two bf16 per column):
+//   warps 0-7  gather the nine [128 tokens x 64] K-chunks of each tile (16-byte
+//              cp.async, manual 128-byte swizzle, a skipped selection is
+//              zero-filled; completion by cp.async.mbarrier.arrive, so no
+//              gathering thread waits) into a 9-slot ring, one slot per chunk;
+//   warps 8-11 softmax, one thread per head: Q row -> TMEM once; per tile read
+//              S, mask skipped selections, keep a lazily moving reference (it
+//              moves only when a score exceeds it by more than 2^8), write P
+//              as bf16 into a K-major 128B-swizzled message buffer with the
+//              tile's O correction factors and running sums, and send the
+//              message to CTA 1 with one shared->shared bulk copy;
+//   warp 12    tcgen05 issuer of S = Q K^T (kind::f16, A = Q from TMEM,
+//              M = 128 heads, N = 128 tokens, K = 576).
+//  CTA 1, the value CTA (TMEM: O [128 heads x 512] f32, all 512 columns):
+//   warps 0-7  gather the eight [128 tokens x 64] value chunks of each tile
+//              (the latent lines the score CTA read a tile earlier: L2 hits);
+//   warps 8-11 rescale O when a message says the reference moved, and write
+//              the normalised output at the end;
+//   warp 12    tcgen05 issuer of O += P V (A = P from the message, K-major;
+//              V MN-major from the ring, N = 128 per pair of chunks), whose
+//              completion frees the message buffer in both CTAs (multicast
+//              commit) and the ring slots.
+// With more than one split the pair writes unnormalised partial O plus its
 // (max, sum) and a combine kernel merges them.
 #include <cuda_bf16.h>
 
@@ -41,22 +45,62 @@ namespace dsa {
 namespace {
 
 constexpr int kGatherWarps = 8;
-constexpr int kThreads = 32 * (kGatherWarps + 4 + 2);  // gather, softmax, S MMA, PV MMA
-constexpr int kMmaWarp = kGatherWarps + 4;
-constexpr int kPvWarp = kMmaWarp + 1;
-constexpr int kRing = 5;
+constexpr int kSoftWarp = kGatherWarps;     // warps 8-11: softmax (CTA 0) / O warps (CTA 1)
+constexpr int kMmaWarp = kGatherWarps + 4;  // warp 12: MMA issuer; owns the TMEM allocation
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kTile = 128;
-constexpr int kChunks = 9;  // 576 / 64
+constexpr int kChunksS = 9;  // 576 / 64: K-chunks per tile (score CTA)
+constexpr int kChunksV = 8;  // 512 / 64: value chunks per tile (value CTA)
 constexpr int kHeads = 128;
 constexpr int kDqk = 576;
-constexpr int kHalf = 256;
+constexpr int kHalf = 256;   // columns of one partial-O block of the combine kernel
 constexpr int kTargetCtas = 152;
 constexpr uint32_t kChunkBytes = kTile * 128;  // 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// TMEM columns.
+constexpr uint32_t kSCol = 0;    // score CTA: S tile
+constexpr uint32_t kQCol = 128;  // score CTA: Q (288 columns)
+constexpr uint32_t kTmemCols = 512;
+
+// Message score CTA -> value CTA for one tile: P [128 heads x 128 tokens] bf16
+// as two K-major 128B-swizzled chunks (tokens 0-63, 64-127), the factor O
+// must be multiplied by before this tile's P V, the running sum after it, and
+// one "reference moved" flag per softmax warp.
+constexpr uint32_t kMsgCorr = 2 * kChunkBytes;
+constexpr uint32_t kMsgL = kMsgCorr + 4 * kHeads;
+constexpr uint32_t kMsgFlags = kMsgL + 4 * kHeads;
+constexpr uint32_t kMsgBytes = kMsgFlags + 16;
+constexpr uint32_t kMsgStride = 34 * 1024;  // keeps the P chunks 1024-byte aligned
+static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message layout");
+
+// Shared memory: a header of barriers at the same offset in both CTAs (the
+// multicast commit names a barrier by its offset), then each CTA's payload.
+struct Header {
+  uint64_t full[kChunksS], empty[kChunksS];  // ring slots (one per chunk of a tile)
+  uint64_t s_full, s_free, q_ready;          // score CTA: S tile written / read, Q in TMEM
+  uint64_t p_full[2], p_free[2];             // message buffer b: arrived / consumed by P V
+  uint64_t need_fix, o_fixed, drain;         // value CTA: O rescale hand-off, final drain
+  uint32_t tmem_base;
+  int abort;
+  int t_fix;  // tile whose P V waits for an O rescale, or -1 = no more tiles
+};
+constexpr uint32_t kHeaderBytes = 1024;
+static_assert(sizeof(Header) <= kHeaderBytes, "header");
+constexpr uint32_t kScoreRing = 0;
+constexpr uint32_t kScoreMsg = kChunksS * kChunkBytes;
+constexpr uint32_t kValueMsg = 0;
+constexpr uint32_t kValueRing = 2 * kMsgStride;
+constexpr uint32_t kScorePayload = kScoreMsg + 2 * kMsgStride;
+constexpr uint32_t kValuePayload = kValueRing + kChunksV * kChunkBytes;
+constexpr uint32_t kPayloadBytes = kScorePayload > kValuePayload ? kScorePayload : kValuePayload;
+constexpr size_t kSmemBytes = 1024 + kHeaderBytes + kPayloadBytes;
+static_assert(kSmemBytes <= 227 * 1024, "sparse MLA shared memory exceeds 227 KB");
+
 struct MParams {
+  const uint16_t* q;  // [R, 128, 576] bf16
   const uint8_t* kv;  // latent cache base: row r (page*64 + slot) at kv + r * 1152
   const int32_t* bt;
   int64_t bt_stride;
@@ -75,26 +119,13 @@ struct MParams {
   uint32_t* err;
 };
 
-struct MSmem {
-  uint8_t q[kChunks][kHeads * 128];  // 9 x 16 KB, K-major SW128, rows = heads
-  uint8_t ring[kRing][kChunkBytes];  // [128 tokens x 64 elems] bf16 SW128
-  uint64_t q_full;
-  // a slot's use is signalled on full[] (an S chunk) or fullv[] (a value
-  // chunk): each barrier has one consumer thread, which waits every phase
-  // in order, so a parity wait cannot pass on an older phase
-  uint64_t full[kRing], fullv[kRing], empty[kRing];
-  uint64_t s_full[2];
-  uint64_t p_full[2], pv_done[2];  // per S/P tile: tile t uses index t & 1
-  uint32_t tmem_base;
-  int abort;
-};
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 // 2^x by the hardware approximation (a few ulp; P is rounded to bf16 anyway).
 // 2^-inf = 0.
@@ -103,28 +134,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const MParams p) {
-  constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kIdescS = make_idesc(1, 1, 128, kTile, false, false);
-  constexpr int kSCol = 0;    // S/P tiles at columns [0, 256)
-  constexpr int kOCol = 256;  // O half at columns [256, 512)
+// Partial block of (row, value half vh, split) for the combine kernel:
+// 128 x 256 O, then 128 maxima, then 128 sums.
+__device__ __forceinline__ float* partial_block(const MParams& p, int row, int vh, int split) {
+  return p.ws + ((static_cast<int64_t>(row) * 2 + vh) * p.nsplit + split) *
+                    (kHeads * kHalf + 2 * kHeads);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MParams p) {
   extern __shared__ uint8_t smem_raw[];
-  MSmem& s = *reinterpret_cast<MSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                       ~uintptr_t(1023));
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Header& s = *reinterpret_cast<Header*>(base);
+  uint8_t* pay = base + kHeaderBytes;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int row = blockIdx.x;
-  const int vh = blockIdx.y;
-  const int split = blockIdx.z;
+  const uint32_t rank = cluster_ctarank();  // 0 = score CTA, 1 = value CTA
+  const int row = blockIdx.x >> 1;
+  const int split = blockIdx.y;
   // the block-table row of this query row (an out-of-range one reads nothing)
   int req = p.row_bt ? p.row_bt[row] : row / p.next_n;
   if (p.row_bt && (req < 0 || req >= p.bt_num_rows)) {
-    if (threadIdx.x == 0) raise_error(p.err, kErrBadPage);
+    if (tid == 0 && rank == 0) raise_error(p.err, kErrBadPage);
     req = -1;
   }
   const int s0 = split * p.tokens_per_split;
@@ -134,41 +168,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     s.abort = 0;
-    mbar_init(&s.q_full, 1);
-    for (int i = 0; i < kRing; ++i) {
+    s.t_fix = 0;
+    for (int i = 0; i < kChunksS; ++i) {
       mbar_init(&s.full[i], 32 * kGatherWarps);  // one cp.async completion per gather thread
-      mbar_init(&s.fullv[i], 32 * kGatherWarps);
-      mbar_init(&s.empty[i], 1);
+      mbar_init(&s.empty[i], 1);                 // the MMA issuer's commit
     }
-    mbar_init(&s.s_full[0], 1);
-    mbar_init(&s.s_full[1], 1);
-    // One arrival per softmax warp, one barrier per S/P tile: a warp can run one
-    // tile ahead of the others (S(i+1) does not wait for P(i)), never two (S(i+2)
-    // waits for PV(i)), so its arrival never lands in another tile's phase.
-    mbar_init(&s.p_full[0], 4);
-    mbar_init(&s.p_full[1], 4);
-    // PV(t) commits to pv_done[t & 1].  With one barrier per tile parity every
-    // waiter is within one phase of the phase it waits for (S(i) is issued only
-    // after PV(i-2) completed), so a parity wait cannot alias an older phase.
-    mbar_init(&s.pv_done[0], 1);
-    mbar_init(&s.pv_done[1], 1);
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.s_free, 4);   // the 4 softmax warps have read S
+    mbar_init(&s.q_ready, 4);  // the 4 softmax warps have stored their Q rows
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.p_full[b], 1);  // the score CTA's remote arrive (+ the copy's bytes)
+      mbar_init(&s.p_free[b], 1);  // the value CTA's multicast commit
+    }
+    mbar_init(&s.need_fix, 1);
+    mbar_init(&s.o_fixed, 4);
+    mbar_init(&s.drain, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  // both CTAs' barriers are initialised before any remote arrival or copy
+  cluster_sync_all();
   tc_fence_after();
   volatile int* abort = &s.abort;
+  const uint32_t tmem = s.tmem_base;
 
   if (warp < kGatherWarps) {
     // -------------------------------------------------------------- gather --
+    const int nch = rank == 0 ? kChunksS : kChunksV;
+    uint8_t* ring = pay + (rank == 0 ? kScoreRing : kValueRing);
     const int gt = tid;  // 0 .. 32*kGatherWarps-1
-    if (gt == 0 && ntile > 0) {
-      tma_prefetch_desc(&tm_q);
-      mbar_arrive_expect_tx(&s.q_full, kChunks * kHeads * 128);
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_2d(s.q[c], &tm_q, &s.q_full, 64 * c, row * kHeads);
-    }
     // Thread gt copies, of every 16 KB chunk, the 16-byte pieces gt + 256 q
     // (q = 0..3): chunk row (gt >> 3) + 32 q, piece gt & 7.  Its 4 latent rows
     // (page*64 + slot, -1 = skipped) of tile i+1 are computed while tile i is
@@ -196,11 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         r[u] = -1;
         if (t[u] >= 0) {
           if (pg[u] >= 0 && pg[u] < p.num_pages) r[u] = pg[u] * 64 + t[u] % 64;
-          else if (pch == 0) raise_error(p.err, kErrBadIndex);
+          else if (pch == 0 && rank == 0) raise_error(p.err, kErrBadIndex);
         }
       }
     };
-    int tk_next[4], rows_cur[4], rows_prev[4] = {-1, -1, -1, -1};
+    int tk_next[4], rows_cur[4];
     {
       int t0[4], pg0[4];
       load_toks(0, t0);
@@ -208,26 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       make_rows(t0, pg0, rows_cur);
       load_toks(1, tk_next);
     }
-    int g = 0;  // ring sequence number
     bool bad = false;
-    auto issue = [&](int c, const int (&r)[4], bool value) -> bool {
-      const int slot = g % kRing;
-      if (g >= kRing && !mbar_wait_warp(&s.empty[slot], ((g / kRing) - 1) & 1, p.err, abort))
-        return false;
-      uint8_t* dst = s.ring[slot];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint8_t* d = dst + sw128_offset(prow + kRowStep * u, pch);
-        if (r[u] >= 0)
-          cp_async_16(d, p.kv + static_cast<int64_t>(r[u]) * (kDqk * 2) + c * 128 + pch * 16);
-        else
-          cp_async_16_zero(d, p.kv);
-      }
-      cp_async_mbar_arrive_noinc(value ? &s.fullv[slot] : &s.full[slot]);
-      ++g;
-      return true;
-    };
-    for (int i = 0; i <= ntile && !bad; ++i) {
+    for (int i = 0; i < ntile && !bad; ++i) {
       // loads for the next tiles go out first; their results are used after
       // this tile's copies have been issued
       int pg_next[4] = {-1, -1, -1, -1}, tk_after[4] = {-1, -1, -1, -1};
@@ -235,110 +246,149 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_pages(tk_next, pg_next);
         load_toks(i + 2, tk_after);
       }
-      if (i < ntile)
-        for (int c = 0; c < kChunks && !bad; ++c) bad = !issue(c, rows_cur, false);
-      if (i >= 1)
-        for (int j = 0; j < 4 && !bad; ++j) bad = !issue(4 * vh + j, rows_prev, true);
+      for (int c = 0; c < nch; ++c) {
+        // slot c held chunk c of tile i-1 until its MMAs completed
+        if (i > 0 && !mbar_wait_warp(&s.empty[c], (i - 1) & 1, p.err, abort)) { bad = true; break; }
+        uint8_t* dst = ring + c * kChunkBytes;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint8_t* d = dst + sw128_offset(prow + kRowStep * u, pch);
+          if (rows_cur[u] >= 0)
+            cp_async_16(d, p.kv + static_cast<int64_t>(rows_cur[u]) * (kDqk * 2) + c * 128 + pch * 16);
+          else
+            cp_async_16_zero(d, p.kv);
+        }
+        cp_async_mbar_arrive_noinc(&s.full[c]);
+      }
       int rows_next[4] = {-1, -1, -1, -1};
       if (i + 1 < ntile) make_rows(tk_next, pg_next, rows_next);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        rows_prev[u] = rows_cur[u];
         rows_cur[u] = rows_next[u];
         tk_next[u] = tk_after[u];
       }
     }
     cp_async_wait<0>();  // no copy of this thread is left in flight at exit
   } else if (warp == kMmaWarp) {
-    // -------------------------------------------------------- S MMA issuer --
-    // One thread runs each MMA role: an M=128 MMA holds the issuing thread for
-    // ~96-128 cycles, longer than the tensor core needs for it, so S (this
-    // warp) and P V (the next warp) are issued by two threads.  Their MMAs
-    // touch disjoint TMEM (S(i+1) its tile, PV(i) P(i) and O), and each
-    // thread's commits track only its own MMAs.  Ring order: S(0), then per
-    // tile i >= 1 S(i) followed by PV(i-1), and PV(ntile-1) last; S(i) starts
-    // at ring sequence number 13 i - 4 (i >= 1).
-    if (lane == 0 && ntile > 0 && mbar_wait(&s.q_full, 0, p.err, abort)) {
-      uint32_t phase = 0;  // bit j: parity of the next phase of full[j]
-      for (int i = 0; i < ntile && !*abort; ++i) {
-        bool bad = false;
-        int g = i == 0 ? 0 : (kChunks + 4) * i - 4;
-        {
-          const int buf = i & 1;
-          // the S/P tile is reused after PV(i-2) has read P(i-2) from it
-          if (i >= 2 && !mbar_wait(&s.pv_done[i & 1], ((i - 2) >> 1) & 1, p.err, abort)) break;
+    if (rank == 0) {
+      // ------------------------------------------------------ S MMA issuer --
+      // One thread; S(i) overwrites the S tile once the softmax has read S(i-1).
+      constexpr uint32_t kIdescS = make_idesc(1, 1, 128, kTile, false, false);
+      const uint8_t* ring = pay + kScoreRing;
+      if (lane == 0 && ntile > 0 && mbar_wait(&s.q_ready, 0, p.err, abort)) {
+        tc_fence_after();
+        for (int i = 0; i < ntile && !*abort; ++i) {
+          if (i > 0 && !mbar_wait(&s.s_free, (i - 1) & 1, p.err, abort)) break;
           tc_fence_after();
-          const uint32_t dS = s.tmem_base + kSCol + buf * kTile;
-          for (int c = 0; c < kChunks; ++c, ++g) {
-            const int slot = g % kRing;
-            if (!mbar_wait(&s.full[slot], (phase >> slot) & 1, p.err, abort)) { bad = true; break; }
-            phase ^= 1u << slot;
+          bool bad = false;
+          for (int c = 0; c < kChunksS; ++c) {
+            if (!mbar_wait(&s.full[c], i & 1, p.err, abort)) { bad = true; break; }
             fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core
             tc_fence_after();
-            const uint32_t a0 = smem_u32(s.q[c]);
-            const uint32_t b0 = smem_u32(s.ring[slot]);
+            const uint32_t b0 = smem_u32(ring + c * kChunkBytes);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16(dS, sw128_desc(a0 + 32 * kk, 16, 1024), sw128_desc(b0 + 32 * kk, 16, 1024),
-                      kIdescS, (c | kk) != 0);
-            mma_commit(&s.empty[slot]);
+              mma_f16_ts(tmem + kSCol, tmem + kQCol + 32 * c + 8 * kk,
+                         sw128_desc(b0 + 32 * kk, 16, 1024), kIdescS, (c | kk) != 0);
+            mma_commit(&s.empty[c]);
           }
           if (bad) break;
-          mma_commit(&s.s_full[buf]);
+          mma_commit(&s.s_full);
         }
       }
-    }
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    // ------------------------------------------------------- PV MMA issuer --
-    // PV(t) reads ring sequence numbers 13 t + 18 .. (after S(t+1)), or
-    // 13 t + 9 .. for the last tile.
-    if (lane == 0 && ntile > 0) {
-      uint32_t phase = 0;  // bit j: parity of the next phase of fullv[j]
-      for (int t = 0; t < ntile && !*abort; ++t) {
-        bool bad = false;
-        const int g = t + 1 < ntile ? (kChunks + 4) * t + 18 : (kChunks + 4) * t + kChunks;
-        {
-          if (!mbar_wait(&s.p_full[t & 1], (t >> 1) & 1, p.err, abort)) break;
-          for (int j = 0; j < 4 && !bad; ++j) {
-            const int gg = g + j;
-            const int slot = gg % kRing;
-            bad = !mbar_wait(&s.fullv[slot], (phase >> slot) & 1, p.err, abort);
-            phase ^= 1u << slot;
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------ PV MMA issuer --
+      // O[:, 128 j2 .. +128] += P V_j2 per pair j2 of value chunks (N = 128);
+      // each pair's ring slots are freed as soon as its MMAs complete, so the
+      // next tile's gathers start while this tile's later pairs run.
+      constexpr uint32_t kIdescPV = make_idesc(1, 1, 128, 128, false, true);
+      const uint8_t* msg0 = pay + kValueMsg;
+      const uint8_t* ring = pay + kValueRing;
+      if (lane == 0) {
+        int nfix = 0;
+        for (int t = 0; t < ntile && !*abort; ++t) {
+          const int b = t & 1;
+          const uint8_t* msg = msg0 + b * kMsgStride;
+          if (!mbar_wait_cluster(&s.p_full[b], (t >> 1) & 1, p.err, abort)) break;
+          const uint32_t* fl = reinterpret_cast<const uint32_t*>(msg + kMsgFlags);
+          if ((fl[0] | fl[1] | fl[2] | fl[3]) != 0) {
+            // the reference moved: O (through P V of tile t-1) is rescaled first
+            *reinterpret_cast<volatile int*>(&s.t_fix) = t;
+            mbar_arrive(&s.need_fix);
+            if (!mbar_wait(&s.o_fixed, nfix & 1, p.err, abort)) break;
+            ++nfix;
           }
-          if (bad) break;
-          fence_proxy_async_smem();
-          tc_fence_after();
-          // value chunk j sits in slot (g + j) % kRing: one or two contiguous runs
-          const int first = g % kRing;
-          const int n1 = min(4, kRing - first);  // chunks in the first run
-          const uint32_t pa = s.tmem_base + kSCol + (t & 1) * kTile;
-          const uint32_t v0 = smem_u32(s.ring[first]);
-          const uint32_t v1 = smem_u32(s.ring[0]);
+          bool bad = false;
+          const uint32_t pa = smem_u32(msg);
+          for (int j2 = 0; j2 < kChunksV / 2 && !bad; ++j2) {
+            for (int c = 2 * j2; c < 2 * j2 + 2; ++c)
+              if (!mbar_wait(&s.full[c], t & 1, p.err, abort)) { bad = true; break; }
+            if (bad) break;
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint32_t v0 = smem_u32(ring + 2 * j2 * kChunkBytes);
 #pragma unroll 1
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-            mma_f16_ts(s.tmem_base + kOCol, pa + 8 * kk,
-                       sw128_desc(v0 + 2048 * kk, kChunkBytes, 1024),
-                       make_idesc(1, 1, 128, 64 * n1, false, true), acc);
-            if (n1 < 4)
-              mma_f16_ts(s.tmem_base + kOCol + 64 * n1, pa + 8 * kk,
-                         sw128_desc(v1 + 2048 * kk, kChunkBytes, 1024),
-                         make_idesc(1, 1, 128, 64 * (4 - n1), false, true), acc);
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_f16(tmem + 128 * j2,
+                      sw128_desc(pa + (kk >> 2) * kChunkBytes + 32 * (kk & 3), 16, 1024),
+                      sw128_desc(v0 + 2048 * kk, kChunkBytes, 1024), kIdescPV,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&s.empty[2 * j2]);
+            mma_commit(&s.empty[2 * j2 + 1]);
           }
-          for (int j = 0; j < 4; ++j) mma_commit(&s.empty[(g + j) % kRing]);
-          mma_commit(&s.pv_done[t & 1]);
+          if (bad) break;
+          // message buffer b is free again in both CTAs once these MMAs complete
+          mma_commit_mc(&s.p_free[b], 0x3);
         }
+        *reinterpret_cast<volatile int*>(&s.t_fix) = -1;
+        mbar_arrive(&s.need_fix);
+        // every MMA of this thread (and its arrivals in the score CTA) completes
+        // before the pair leaves
+        mma_commit(&s.drain);
+        mbar_wait(&s.drain, 0, p.err, abort);
       }
+      __syncwarp();
     }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------ softmax / epilogue --
-    const int quad = warp & 3;  // warps 8-11: TMEM lane quadrants 0-3
+  } else if (rank == 0) {
+    // ----------------------------------------------------------- softmax --
+    const int quad = warp & 3;       // warps 8-11: TMEM lane quadrants 0-3
     const int h = quad * 32 + lane;  // head == TMEM lane
-    const uint32_t lane_base = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool leader = warp == kSoftWarp && lane == 0;
+    uint8_t* msg0 = pay + kScoreMsg;
+    const uint32_t peer_msg0 = mapa_shared(smem_u32(pay + kValueMsg), 1);
     float m_run = -INFINITY, l_run = 0.f;
     bool bad = false;
+    if (ntile > 0) {
+      // Q row of this head -> TMEM columns [kQCol, kQCol + 288): column j holds
+      // elements 2j (low half) and 2j + 1
+      const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(
+          p.q + (static_cast<int64_t>(row) * kHeads + h) * kDqk);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 9; c0 += 3) {
+        uint4 v[3][8];
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[j][u] = ldg_nc_u4(qsrc + (c0 + j) * 128 + 16 * u);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          uint32_t r[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            r[4 * u] = v[j][u].x;
+            r[4 * u + 1] = v[j][u].y;
+            r[4 * u + 2] = v[j][u].z;
+            r[4 * u + 3] = v[j][u].w;
+          }
+          tmem_st32_sync(lane_base + kQCol + 32 * (c0 + j), r);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.q_ready);
+    }
     // validity of a tile's 128 selections: lane j of every warp reads entries
     // j, 32+j, 64+j, 96+j; four ballots give the tile's mask (read a tile ahead)
     auto load_sel = [&](int i, int (&v)[4]) {
@@ -356,22 +406,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 4; ++u) m[u] = __ballot_sync(0xffffffffu, sel[u] >= 0);
       load_sel(i + 1, sel);
       const bool all_valid = (m[0] & m[1] & m[2] & m[3]) == 0xffffffffu;  // warp-uniform
-      const int buf = i & 1;
-      if (!mbar_wait_warp(&s.s_full[buf], (i >> 1) & 1, p.err, abort)) { bad = true; break; }
-      tc_fence_after();
-      const uint32_t sbase = lane_base + kSCol + buf * kTile;
+      const int b = i & 1;
+      uint8_t* msg = msg0 + b * kMsgStride;
+      const bool ok = mbar_wait_warp(&s.s_full, i & 1, p.err, abort);
+      if (ok) tc_fence_after();
+      // message buffer b is rewritten only after the copy of tile i-2 has read it
+      if (leader && ok) bulk_wait_group_read<1>();
+      if (named_bar_or(1, 128, !ok)) { bad = true; break; }
       // One pass over the tile's scores (log2 units, -inf if skipped), 64
       // columns at a time.  P = 2^(x - m_t) against the running reference m_t,
       // which only moves when a score exceeds it by more than the threshold
       // (then P already written for this tile is brought to the new m_t).
-      // P is packed bf16 over the first 64 columns of this S tile: tokens
-      // 0..63 -> columns 0..31 (their scores are read before anything is
-      // written), then tokens 64..127 -> columns 32..63.
       float m_t = m_run, l_t = 0.f;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         float v[64];
-        tmem_ld64_sync(sbase + 64 * half, v);
+        tmem_ld64_sync(lane_base + kSCol + 64 * half, v);
+        if (half == 1) {
+          // the whole S tile is in registers: S(i+1) may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.s_free);
+        }
         float h4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (all_valid) {
 #pragma unroll
@@ -383,30 +439,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             const int t = 64 * half + j;
-            const bool ok = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
-            v[j] = ok ? v[j] * p.scale_log2 : -INFINITY;
+            const bool okj = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
+            v[j] = okj ? v[j] * p.scale_log2 : -INFINITY;
             h4[j & 3] = fmaxf(h4[j & 3], v[j]);
           }
         }
         const float hm = fmaxf(fmaxf(h4[0], h4[1]), fmaxf(h4[2], h4[3]));
         const bool grow = hm > m_t + kRescaleThreshold || (m_t == -INFINITY && hm > -INFINITY);
-        if (__any_sync(0xffffffffu, grow)) {
-          const float m_new = grow ? hm : m_t;
-          if (half == 1) {
-            // bring this tile's first 32 columns of P to the new reference
-            const float f = (grow && m_t > -INFINITY) ? ex2_approx(m_t - m_new) : 1.f;
-            float qf[32];
-            tmem_ld32_sync(sbase, qf);
-            uint32_t q[32];
+        if (grow) {
+          if (half == 1 && m_t > -INFINITY) {
+            // bring this head's P of tokens 0..63 (chunk 0) to the new reference
+            const float f = ex2_approx(m_t - hm);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const uint32_t w = __float_as_uint(qf[j]);
-              q[j] = pack_bf16(bf16_lo(w) * f, bf16_hi(w) * f);
+            for (int q = 0; q < 8; ++q) {
+              uint4* ptr = reinterpret_cast<uint4*>(msg + sw128_offset(h, q));
+              uint4 w = *ptr;
+              w.x = pack_bf16(bf16_lo(w.x) * f, bf16_hi(w.x) * f);
+              w.y = pack_bf16(bf16_lo(w.y) * f, bf16_hi(w.y) * f);
+              w.z = pack_bf16(bf16_lo(w.z) * f, bf16_hi(w.z) * f);
+              w.w = pack_bf16(bf16_lo(w.w) * f, bf16_hi(w.w) * f);
+              *ptr = w;
             }
-            tmem_st32_sync(sbase, q);
             l_t *= f;
           }
-          m_t = m_new;
+          m_t = hm;
         }
         // m_t is -inf only while every score seen is -inf: those give P = 0
         const float mref = m_t == -INFINITY ? 0.f : m_t;
@@ -420,92 +476,134 @@ __global__ void __launch_bounds__(kThreads, 1)
           l4[j & 3] += e0 + e1;  // the exact weights (P itself is rounded to bf16)
         }
         l_t += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-        tmem_st32_sync(sbase + 32 * half, pk);
+        // row h of chunk `half`: tokens 8q .. 8q+7 of the half in 16-byte piece q
+        uint8_t* chunk = msg + half * kChunkBytes;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(chunk + sw128_offset(h, q)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
-      // O and l hold earlier tiles against m_run: bring them to m_t
+      // O and l hold earlier tiles against m_run: they are brought to m_t
       const bool moved = m_t != m_run && m_run > -INFINITY;
       const float corr = moved ? ex2_approx(m_run - m_t) : 1.f;
-      if (__any_sync(0xffffffffu, moved)) {
-        // O must hold PV(i-1) complete before it is rescaled
-        if (!mbar_wait_warp(&s.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err, abort)) { bad = true; break; }
-        tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < kHalf / 32; ++cc) {
-          float o[32];
-          tmem_ld32_sync(lane_base + kOCol + 32 * cc, o);
-          uint32_t r[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(o[j] * corr);
-          tmem_st32_sync(lane_base + kOCol + 32 * cc, r);
-        }
-      }
       l_run = l_run * corr + l_t;
       m_run = m_t;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.p_full[buf]);
-    }
-    // ---- epilogue: O half of this CTA ----
-    if (!bad && ntile > 0 &&
-        mbar_wait_warp(&s.pv_done[(ntile - 1) & 1], ((ntile - 1) >> 1) & 1, p.err, abort)) {
-      tc_fence_after();
-      if (p.nsplit == 1) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint16_t* orow = p.out + (static_cast<int64_t>(row) * kHeads + h) * 512 + vh * kHalf;
-#pragma unroll 1
-        for (int cc = 0; cc < kHalf / 32; ++cc) {
-          float o[32];
-          tmem_ld32_sync(lane_base + kOCol + 32 * cc, o);
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 v;
-            v.x = pack_bf16(o[j] * inv, o[j + 1] * inv);
-            v.y = pack_bf16(o[j + 2] * inv, o[j + 3] * inv);
-            v.z = pack_bf16(o[j + 4] * inv, o[j + 5] * inv);
-            v.w = pack_bf16(o[j + 6] * inv, o[j + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + 32 * cc + j) = v;
-          }
+      reinterpret_cast<float*>(msg + kMsgCorr)[h] = corr;
+      reinterpret_cast<float*>(msg + kMsgL)[h] = l_run;
+      const bool wmoved = __any_sync(0xffffffffu, moved);
+      if (lane == 0) reinterpret_cast<uint32_t*>(msg + kMsgFlags)[quad] = wmoved ? 1u : 0u;
+      fence_proxy_async_smem();  // generic writes -> the bulk copy (async proxy)
+      named_bar_sync(1, 128);
+      if (leader) {
+        // the value CTA's buffer b is free once P V of tile i-2 has completed
+        if (i < 2 || mbar_wait_cluster(&s.p_free[b], ((i - 2) >> 1) & 1, p.err, abort)) {
+          const uint32_t pbar = mapa_shared(smem_u32(&s.p_full[b]), 1);
+          mbar_arrive_expect_tx_remote(pbar, kMsgBytes);
+          bulk_copy_s2s(peer_msg0 + b * kMsgStride, msg, kMsgBytes, pbar);
+          bulk_commit_group();
         }
-        if (vh == 0 && p.lse)
+      }
+      __syncwarp();
+    }
+    if (leader) {
+      bulk_wait_group<0>();
+      // the value CTA's last commits arrive here too: they land before the pair exits
+      for (int t = max(0, ntile - 2); t < ntile && !bad; ++t)
+        if (!mbar_wait_cluster(&s.p_free[t & 1], (t >> 1) & 1, p.err, abort)) break;
+    }
+    __syncwarp();
+    if (!bad) {
+      if (p.nsplit == 1) {
+        if (p.lse)
           p.lse[static_cast<int64_t>(row) * kHeads + h] =
               l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       } else {
-        // partial: [row][vh][split] blocks of (128 x 256 O, 128 m, 128 l)
-        float* blk = p.ws + ((static_cast<int64_t>(row) * 2 + vh) * p.nsplit + split) *
-                                (kHeads * kHalf + 2 * kHeads);
-        float* orow = blk + h * kHalf;
-#pragma unroll 1
-        for (int cc = 0; cc < kHalf / 32; ++cc) {
-          float o[32];
-          tmem_ld32_sync(lane_base + kOCol + 32 * cc, o);
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(orow + 32 * cc + j) =
-                make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        for (int vh = 0; vh < 2; ++vh) {
+          float* blk = partial_block(p, row, vh, split);
+          blk[kHeads * kHalf + h] = m_run;
+          blk[kHeads * kHalf + kHeads + h] = l_run;
         }
-        blk[kHeads * kHalf + h] = m_run;
-        blk[kHeads * kHalf + kHeads + h] = l_run;
       }
-    } else if (ntile == 0) {
-      if (p.nsplit == 1) {
-        uint16_t* orow = p.out + (static_cast<int64_t>(row) * kHeads + h) * 512 + vh * kHalf;
-        for (int j = 0; j < kHalf; j += 8)
-          *reinterpret_cast<uint4*>(orow + j) = make_uint4(0, 0, 0, 0);
-        if (vh == 0 && p.lse) p.lse[static_cast<int64_t>(row) * kHeads + h] = -INFINITY;
-      } else {
-        float* blk = p.ws + ((static_cast<int64_t>(row) * 2 + vh) * p.nsplit + split) *
-                                (kHeads * kHalf + 2 * kHeads);
-        blk[kHeads * kHalf + h] = -INFINITY;
-        blk[kHeads * kHalf + kHeads + h] = 0.f;
+    }
+  } else {
+    // ------------------------------------------------- O rescale / epilogue --
+    const int quad = warp & 3;
+    const int h = quad * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint8_t* msg0 = pay + kValueMsg;
+    bool bad = false;
+    for (int k = 0;; ++k) {
+      if (!mbar_wait_warp(&s.need_fix, k & 1, p.err, abort)) { bad = true; break; }
+      const int tf = *reinterpret_cast<volatile int*>(&s.t_fix);
+      if (tf < 0) break;
+      if (tf >= 1) {
+        // O must hold P V of tile tf-1 complete before it is rescaled
+        const int tp = tf - 1;
+        if (!mbar_wait_warp(&s.p_free[tp & 1], (tp >> 1) & 1, p.err, abort)) { bad = true; break; }
+        tc_fence_after();
+        const float corr =
+            reinterpret_cast<const float*>(msg0 + (tf & 1) * kMsgStride + kMsgCorr)[h];
+#pragma unroll 1
+        for (int cc = 0; cc < 512 / 32; ++cc) {
+          float o[32];
+          tmem_ld32_sync(lane_base + 32 * cc, o);
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(o[j] * corr);
+          tmem_st32_sync(lane_base + 32 * cc, r);
+        }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.o_fixed);
+    }
+    if (!bad && ntile > 0) {
+      const int tl = ntile - 1;
+      if (mbar_wait_warp(&s.p_free[tl & 1], (tl >> 1) & 1, p.err, abort)) {
+        tc_fence_after();
+        const float lr = reinterpret_cast<const float*>(msg0 + (tl & 1) * kMsgStride + kMsgL)[h];
+        if (p.nsplit == 1) {
+          const float inv = lr > 0.f ? 1.f / lr : 0.f;
+          uint16_t* orow = p.out + (static_cast<int64_t>(row) * kHeads + h) * 512;
+#pragma unroll 1
+          for (int cc = 0; cc < 512 / 32; ++cc) {
+            float o[32];
+            tmem_ld32_sync(lane_base + 32 * cc, o);
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 v;
+              v.x = pack_bf16(o[j] * inv, o[j + 1] * inv);
+              v.y = pack_bf16(o[j + 2] * inv, o[j + 3] * inv);
+              v.z = pack_bf16(o[j + 4] * inv, o[j + 5] * inv);
+              v.w = pack_bf16(o[j + 6] * inv, o[j + 7] * inv);
+              *reinterpret_cast<uint4*>(orow + 32 * cc + j) = v;
+            }
+          }
+        } else {
+          // unnormalised partial O: columns [256 vh, 256 vh + 256) into block vh
+#pragma unroll 1
+          for (int cc = 0; cc < 512 / 32; ++cc) {
+            float o[32];
+            tmem_ld32_sync(lane_base + 32 * cc, o);
+            float* orow = partial_block(p, row, cc >> 3, split) + h * kHalf + 32 * (cc & 7);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(orow + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+          }
+        }
+      }
+    } else if (!bad && ntile == 0 && p.nsplit == 1) {
+      uint16_t* orow = p.out + (static_cast<int64_t>(row) * kHeads + h) * 512;
+      for (int j = 0; j < 512; j += 8)
+        *reinterpret_cast<uint4*>(orow + j) = make_uint4(0, 0, 0, 0);
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(s.tmem_base, kTmemCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -564,17 +662,8 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   const int ns = choose_nsplit(R, a.k);
   const int tiles = (a.k + kTile - 1) / kTile;
   const int tps = ((tiles + ns - 1) / ns) * kTile;
-  CUtensorMap tq;
-  char msg[128];
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(R) * kHeads};
-    const uint64_t strides[1] = {kDqk * 2};
-    const uint32_t box[2] = {64, 128};
-    if (!encode_tensor_map(&tq, 1, 2, const_cast<uint16_t*>(a.q), dims, strides, box, true, msg,
-                           sizeof(msg)))
-      return cudaErrorInvalidValue;
-  }
   MParams p;
+  p.q = a.q;
   p.kv = reinterpret_cast<const uint8_t*>(a.kv);
   p.bt = a.block_table;
   p.bt_stride = a.bt_stride;
@@ -591,13 +680,25 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   p.lse = a.lse;
   p.ws = static_cast<float*>(a.ws);
   p.err = dev.err_word;
-  const size_t smem = sizeof(MSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+                                       static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
-  sparse_mla_kernel<<<dim3(R, 2, ns), kThreads, smem, stream>>>(tq, p);
-  e = cudaGetLastError();
+  // one cluster of two CTAs (score, value) per (row, split)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * R, ns, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
   mla_combine_kernel<<<dim3(R, 2), 256, 0, stream>>>(p);
   return cudaGetLastError();

@@ -46,6 +46,11 @@ def compare(mla, layout, next_n, idx, out, lse, rows=None, rel=0.0):
     ([700, 3000], 2, 2048, 0.1),            # rows shorter than k (-1 tails) + holes
     ([4000], 1, 100, 0.0),                  # ragged last tile, split-K path
     ([9000, 9000, 9000, 9000], 1, 2048, 0.02),
+    # 40 rows and more: one split per row (no combine), the pair's full
+    # message / rescale protocol over 16 tiles
+    ([3000] * 40, 1, 2048, 0.0),
+    ([700, 3000] * 20, 2, 2048, 0.1),       # -1 tails + holes, 80 rows
+    ([2500] * 48, 1, 300, 0.05),            # ragged last tile, 3 tiles
 ])
 def test_mla_parity(ctx, next_n, k, holes):
     mla, layout, idx, out, lse = run_case(ctx, next_n, k, seed=5, holes=holes)
@@ -72,7 +77,8 @@ def test_mla_index_order_does_not_matter_and_is_not_a_prefix():
     assert (out.float() - out3.float()).abs().max() > 0.05
 
 
-def test_mla_scores_growing_within_and_across_tiles():
+@pytest.mark.parametrize("nreq", [2, 40])
+def test_mla_scores_growing_within_and_across_tiles(nreq):
     """Scores that rise inside a 128-token tile (second half) and from tile to
     tile, so the running softmax reference moves mid-tile (P already written
     for the tile's first half is brought to the new reference) and between
@@ -81,20 +87,20 @@ def test_mla_scores_growing_within_and_across_tiles():
     their unit scale; but each output is then close to a single value row
     (up to ~4.5), so the bound adds one bf16 ulp of the reference (2^-8 |ref|)
     for the rounding of the stored output."""
-    ctx, k = [6000, 7000], 512
+    ctx, k = ([6000, 7000] * nreq)[:nreq], 512
     layout = W.make_layout(ctx, 7, device="cuda")
-    mla = W.make_mla_case(2, layout.num_pages, seed=7, device="cuda")
+    mla = W.make_mla_case(nreq, layout.num_pages, seed=7, device="cuda")
     L = W.row_lengths(layout.ctx_len, 1).tolist()
     idx = W.random_indices(L, k, seed=7, device="cuda")
     kv = mla.kv.float()
     bt = layout.block_table
-    for r in range(2):
+    for r in range(nreq):
         toks = idx[r].long()
         j = torch.arange(k, device="cuda")
         factor = 1.0 + 19.0 * ((j % 128) >= 64).float() + 10.0 * (j // 128).float()
         pages, slots = bt[r, toks // 64].long(), toks % 64
         kv[pages, slots, 512:] *= factor[:, None]
     mla.kv.copy_(kv.to(torch.bfloat16))
-    out, lse = gpu_mla(mla, layout.block_table, 2, 1, idx, layout.num_pages)
+    out, lse = gpu_mla(mla, layout.block_table, nreq, 1, idx, layout.num_pages)
     torch.cuda.synchronize()
     compare(mla, layout, 1, idx, out, lse, rel=2.0 ** -8)
