@@ -14,7 +14,10 @@
 //              cp.async, manual 128-byte swizzle, a skipped selection is
 //              zero-filled; completion by cp.async.mbarrier.arrive, so no
 //              gathering thread waits) into a 9-slot ring, one slot per chunk;
-//   warps 8-11 softmax, one thread per head: Q row -> TMEM once; per tile read
+//   warps 8-11 softmax, one thread per head: Q -> TMEM once (by TMA into
+//              the two idle message buffers, four 16 KB chunks at a time,
+//              then each thread moves its head's row; the gathers' cp.async
+//              path is left to the gathers); per tile read
 //              S, mask skipped selections, keep a lazily moving reference (it
 //              moves only when a score exceeds it by more than 2^8), write P
 //              as bf16 into a K-major 128B-swizzled message buffer with the
@@ -83,6 +86,7 @@ struct Header {
   uint64_t s_full, s_free, q_ready;          // score CTA: S tile written / read, Q in TMEM
   uint64_t p_full[2], p_free[2];             // message buffer b: arrived / consumed by P V
   uint64_t need_fix, o_fixed, drain;         // value CTA: O rescale hand-off, final drain
+  uint64_t q_full;                           // score CTA: a round of Q chunks landed
   uint32_t tmem_base;
   int abort;
   int t_fix;  // tile whose P V waits for an O rescale, or -1 = no more tiles
@@ -142,7 +146,8 @@ __device__ __forceinline__ float* partial_block(const MParams& p, int row, int v
                     (kHeads * kHalf + 2 * kHeads);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const MParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -183,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MParams p
     mbar_init(&s.need_fix, 1);
     mbar_init(&s.o_fixed, 4);
     mbar_init(&s.drain, 1);
+    mbar_init(&s.q_full, 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
@@ -361,33 +367,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MParams p
     float m_run = -INFINITY, l_run = 0.f;
     bool bad = false;
     if (ntile > 0) {
-      // Q row of this head -> TMEM columns [kQCol, kQCol + 288): column j holds
-      // elements 2j (low half) and 2j + 1
-      const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(
-          p.q + (static_cast<int64_t>(row) * kHeads + h) * kDqk);
+      // Q of the row -> TMEM columns [kQCol, kQCol + 288), lane h = head h,
+      // column j holding elements 2j (low half) and 2j + 1: in three rounds
+      // (chunks 0-3, 4-7, 8) TMA puts [128 heads x 64] K-chunks (128B-swizzled)
+      // into the message buffers, idle until tile 0, and each thread copies its
+      // head's row of them into TMEM
+      uint8_t* stage = msg0;  // 4 x 16 KB, 1024-aligned, within the two buffers
+      if (leader) tma_prefetch_desc(&tm_q);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 9; c0 += 3) {
-        uint4 v[3][8];
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[j][u] = ldg_nc_u4(qsrc + (c0 + j) * 128 + 16 * u);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          uint32_t r[32];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            r[4 * u] = v[j][u].x;
-            r[4 * u + 1] = v[j][u].y;
-            r[4 * u + 2] = v[j][u].z;
-            r[4 * u + 3] = v[j][u].w;
-          }
-          tmem_st32_sync(lane_base + kQCol + 32 * (c0 + j), r);
+      for (int rd = 0; rd < 3; ++rd) {
+        const int c0 = 4 * rd, nc = rd < 2 ? 4 : 1;
+        if (leader) {
+          mbar_arrive_expect_tx(&s.q_full, nc * kChunkBytes);
+          for (int j = 0; j < nc; ++j)
+            tma_load_2d(stage + j * kChunkBytes, &tm_q, &s.q_full, 64 * (c0 + j), row * kHeads);
         }
+        __syncwarp();
+        const bool ok = mbar_wait_warp(&s.q_full, rd & 1, p.err, abort);
+        if (ok) {
+          for (int j = 0; j < nc; ++j) {
+            uint32_t r[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint4 w = *reinterpret_cast<const uint4*>(stage + j * kChunkBytes + sw128_offset(h, u));
+              r[4 * u] = w.x;
+              r[4 * u + 1] = w.y;
+              r[4 * u + 2] = w.z;
+              r[4 * u + 3] = w.w;
+            }
+            tmem_st32_sync(lane_base + kQCol + 32 * (c0 + j), r);
+          }
+          fence_proxy_async_smem();  // these reads come before the next round's TMA writes
+        }
+        // every thread has its rows before the buffers are refilled (or reused for P)
+        if (named_bar_or(1, 128, !ok)) { bad = true; break; }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.q_ready);
+      if (!bad && lane == 0) mbar_arrive(&s.q_ready);
     }
     // validity of a tile's 128 selections: lane j of every warp reads entries
     // j, 32+j, 64+j, 96+j; four ballots give the tile's mask (read a tile ahead)
@@ -400,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MParams p
     };
     int sel[4];
     load_sel(0, sel);
-    for (int i = 0; i < ntile; ++i) {
+    for (int i = 0; i < ntile && !bad; ++i) {
       unsigned m[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) m[u] = __ballot_sync(0xffffffffu, sel[u] >= 0);
@@ -608,38 +625,56 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MParams p
 }
 
 // Merges the split partials: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// Grid (row, value half, head group of kCombineHeads); thread t owns output
+// column t of the half for the group's heads, so the loads of all its heads
+// are in flight together (a loop over the 128 heads with one dependent load
+// each was latency-bound: ~60 us at 32 rows x 2 splits).
+constexpr int kCombineHeads = 16;
 __global__ void __launch_bounds__(256) mla_combine_kernel(const MParams p) {
   const int row = blockIdx.x;
   const int vh = blockIdx.y;
+  const int h0 = blockIdx.z * kCombineHeads;
   const int t = threadIdx.x;
   const int64_t blk_floats = kHeads * kHalf + 2 * kHeads;
   const float* base = p.ws + (static_cast<int64_t>(row) * 2 + vh) * p.nsplit * blk_floats;
-  __shared__ float wsh[64][kHeads];  // nsplit <= 64
-  __shared__ float inv_l[kHeads];
-  if (t < kHeads) {
+  __shared__ float wsh[64][kCombineHeads];  // nsplit <= 64
+  __shared__ float inv_l[kCombineHeads];
+  if (t < kCombineHeads) {
+    const int h = h0 + t;
     float M = -INFINITY;
-    for (int sp = 0; sp < p.nsplit; ++sp) M = fmaxf(M, base[sp * blk_floats + kHeads * kHalf + t]);
+    for (int sp = 0; sp < p.nsplit; ++sp) M = fmaxf(M, base[sp * blk_floats + kHeads * kHalf + h]);
     float L = 0.f;
     for (int sp = 0; sp < p.nsplit; ++sp) {
-      const float m = base[sp * blk_floats + kHeads * kHalf + t];
+      const float m = base[sp * blk_floats + kHeads * kHalf + h];
       const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
       wsh[sp][t] = w;
-      L += w * base[sp * blk_floats + kHeads * kHalf + kHeads + t];
+      L += w * base[sp * blk_floats + kHeads * kHalf + kHeads + h];
     }
     inv_l[t] = L > 0.f ? 1.f / L : 0.f;
     if (vh == 0 && p.lse)
-      p.lse[static_cast<int64_t>(row) * kHeads + t] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+      p.lse[static_cast<int64_t>(row) * kHeads + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
   __syncthreads();
-  for (int h = 0; h < kHeads; ++h) {
-    float acc = 0.f;
-    for (int sp = 0; sp < p.nsplit; ++sp) {
-      const float w = wsh[sp][h];
-      if (w != 0.f) acc += w * base[sp * blk_floats + h * kHalf + t];
+  float acc[kCombineHeads];
+#pragma unroll
+  for (int j = 0; j < kCombineHeads; ++j) acc[j] = 0.f;
+  for (int sp = 0; sp < p.nsplit; ++sp) {
+    const float* o = base + sp * blk_floats + static_cast<int64_t>(h0) * kHalf + t;
+    float v[kCombineHeads];
+#pragma unroll
+    for (int j = 0; j < kCombineHeads; ++j) v[j] = o[j * kHalf];
+    // a split with no valid selection has weight 0 and an unwritten O block:
+    // its values are never used
+#pragma unroll
+    for (int j = 0; j < kCombineHeads; ++j) {
+      const float w = wsh[sp][j];
+      if (w != 0.f) acc[j] = fmaf(w, v[j], acc[j]);
     }
-    p.out[(static_cast<int64_t>(row) * kHeads + h) * 512 + vh * kHalf + t] =
-        __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv_l[h]));
   }
+#pragma unroll
+  for (int j = 0; j < kCombineHeads; ++j)
+    p.out[(static_cast<int64_t>(row) * kHeads + h0 + j) * 512 + vh * kHalf + t] =
+        __bfloat16_as_ushort(__float2bfloat16_rn(acc[j] * inv_l[j]));
 }
 
 int choose_nsplit(int R, int k) {
@@ -680,6 +715,18 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   p.lse = a.lse;
   p.ws = static_cast<float*>(a.ws);
   p.err = dev.err_word;
+  CUtensorMap tq;
+  {
+    // q as [R * 128 rows (row-major heads), 576] bf16; one box = a [128 x 64]
+    // K-chunk of a row's Q, 128-byte swizzle
+    char msg[160];
+    const uint64_t dims[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(R) * kHeads};
+    const uint64_t strides[1] = {kDqk * 2};
+    const uint32_t box[2] = {64, kHeads};
+    if (!encode_tensor_map(&tq, 1, 2, const_cast<uint16_t*>(a.q), dims, strides, box, true, msg,
+                           sizeof(msg)))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
@@ -697,10 +744,10 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, tq, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
-  mla_combine_kernel<<<dim3(R, 2), 256, 0, stream>>>(p);
+  mla_combine_kernel<<<dim3(R, 2, kHeads / kCombineHeads), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
