@@ -53,7 +53,7 @@ __host__ __device__ constexpr int stages_for(int) { return 8; }
 constexpr int kTileTokens = 128;
 constexpr uint32_t kPageKeyBytes = 64 * 128;  // 8192
 constexpr uint32_t kStageBytes = 2 * kPageKeyBytes;
-constexpr int kChunkTiles = 4;
+constexpr int kChunkTiles = 8;
 constexpr int kMaxReq = 4096;
 
 struct KParams {
