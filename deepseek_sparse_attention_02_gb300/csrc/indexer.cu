@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  pdl_launch_dependents_and_wait();
 
   // ---- per-request chunk counts and their exclusive prefix (all threads) ----
   for (int i = tid; i < p.num_req; i += kThreads) {
@@ -527,8 +528,16 @@ cudaError_t launch_g(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t s
   p.logits = a.logits;
   p.ld = a.ld;
   p.err = dev.err_word;
-  fn<<<dev.sm_count, kThreads, smem, stream>>>(tk, tq, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(dev.sm_count);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, fn, tk, tq, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace

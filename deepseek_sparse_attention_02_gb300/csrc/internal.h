@@ -16,6 +16,16 @@ struct DeviceInfo {
   uint32_t* err_word = nullptr;  // device address of this device's error word
 };
 
+// Launch attribute for programmatic dependent launch: the kernel may be
+// scheduled while the previous kernel in the stream finishes; it waits for
+// that kernel (griddepcontrol.wait) before it touches global memory.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // Fills `info` for the current device.
 cudaError_t current_device_info(DeviceInfo* info);
 

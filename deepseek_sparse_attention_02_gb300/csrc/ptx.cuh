@@ -343,6 +343,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch: the kernel that follows this one in the
+// stream (when launched with programmatic stream serialization) may be
+// scheduled from now on; and this kernel waits here until the kernel before
+// it has completed and its memory is visible (at once if it was launched
+// without the attribute).  Every kernel of the library calls both before its
+// first global memory access, so only launch latency and CTA placement
+// overlap the previous kernel.
+__device__ __forceinline__ void pdl_launch_dependents_and_wait() {
+  asm volatile("griddepcontrol.launch_dependents;\n\tgriddepcontrol.wait;" ::: "memory");
+}
+
 // Named barrier that also ORs a predicate over the participating threads:
 // every thread gets the same result, so a group that must stop together does.
 __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {

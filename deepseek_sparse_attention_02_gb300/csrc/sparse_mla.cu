@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t rank = cluster_ctarank();  // 0 = score CTA, 1 = value CTA
+  pdl_launch_dependents_and_wait();
   const int row = blockIdx.x >> 1;
   const int split = blockIdx.y;
   // the block-table row of this query row (an out-of-range one reads nothing)
@@ -635,6 +636,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MParams p) {
   const int vh = blockIdx.y;
   const int h0 = blockIdx.z * kCombineHeads;
   const int t = threadIdx.x;
+  pdl_launch_dependents_and_wait();
   const int64_t blk_floats = kHeads * kHalf + 2 * kHeads;
   const float* base = p.ws + (static_cast<int64_t>(row) * 2 + vh) * p.nsplit * blk_floats;
   __shared__ float wsh[64][kCombineHeads];  // nsplit <= 64
@@ -737,18 +739,25 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStrea
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel, tq, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
-  mla_combine_kernel<<<dim3(R, 2, kHeads / kCombineHeads), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3(R, 2, kHeads / kCombineHeads);
+  ccfg.blockDim = dim3(256);
+  ccfg.stream = stream;
+  ccfg.attrs = attr + 1;
+  ccfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&ccfg, mla_combine_kernel, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 // ------------------------------------------------ no-allocation variant --

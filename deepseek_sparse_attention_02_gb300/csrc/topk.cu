@@ -540,6 +540,7 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
   TkSmem& s =
       *reinterpret_cast<TkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
   const int tid = threadIdx.x;
+  pdl_launch_dependents_and_wait();
   // With two CTAs per row (a cluster of two, used when the rows are few) both
   // derive the same cutoff from the row's sample, each compacts half of the
   // row, rank 1 into regions kWarps..2 kWarps-1 of rank 0's shared memory, and
@@ -694,21 +695,30 @@ cudaError_t launch_topk_t(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t
   if (e != cudaSuccess) return e;
   if (!pair) {
     const int grid = a.R < dev.sm_count ? a.R : dev.sm_count;
-    topk_kernel<1, T><<<grid, kT, smem, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_kernel<1, T>, p);
+    return e == cudaSuccess ? cudaGetLastError() : e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a.R);
   cfg.blockDim = dim3(kT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, topk_kernel<2, T>, p);
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
