@@ -28,6 +28,11 @@
  *   workspace whose size the matching *_size query returns.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
  *   only enqueues work and returns; nothing is synchronised.
+ * - The indexer, top-k and sparse-attention kernels are launched with
+ *   programmatic stream serialization: one of them may be placed on the GPU
+ *   while the kernel before it in the stream finishes, but it waits for that
+ *   kernel to complete (and for its writes to be visible) before it reads or
+ *   writes any memory.  Stream order is kept exactly as for plain launches.
  * - Every argument is validated on the host before anything is enqueued; an
  *   unsupported shape or a bad argument returns an error and enqueues nothing.
  *   There is no fallback path.  dsa_last_error() gives a message.
