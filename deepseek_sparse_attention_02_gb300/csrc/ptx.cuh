@@ -105,15 +105,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // L2 policy that marks the lines it is attached to as first to evict: for data
 // read once (a streamed key cache), so that it does not push out data that
 // the next kernel reads again.
@@ -123,7 +114,8 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
-// tma_load_3d with an L2 cache policy attached to the read.
+// 3-D tiled TMA load (one box at coordinates c0, c1, c2) with an L2 cache
+// policy attached to the read.
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
                                                  int c0, int c1, int c2, uint64_t policy) {
   asm volatile(
@@ -134,23 +126,14 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// bulk_load with an L2 cache policy attached to the read.
+// Plain (untiled) bulk copy global -> shared (16-byte aligned, size % 16 == 0)
+// with an L2 cache policy attached to the read.
 __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
                                                uint64_t* bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// Plain (untiled) bulk copy global -> shared; 16-byte aligned, size % 16 == 0.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -171,9 +154,6 @@ __device__ __forceinline__ void cp_async_16_zero(void* dst, const void* any_src)
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(smem_u32(dst)),
                "l"(reinterpret_cast<uint64_t>(any_src))
                : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 // Arrive on the mbarrier once all cp.async issued so far by this thread have
 // completed (the arrival is counted against the barrier's expected count).
@@ -303,7 +283,6 @@ __device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
-
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand whose
 // 8-row x 128-byte swizzle atoms are stacked every `sbo` bytes (1024 for a
@@ -464,13 +443,4 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
   }
 }
-
-__device__ __forceinline__ uint4 ldg_nc_u4(const void* ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr));
-  return v;
-}
-
 }  // namespace dsa
