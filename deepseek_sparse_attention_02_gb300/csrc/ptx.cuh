@@ -443,4 +443,5 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
   }
 }
+
 }  // namespace dsa
