@@ -70,6 +70,7 @@ struct TkSmem {
   uint32_t counter;       // output cursor
   uint32_t bin, above, binc;
   uint32_t ncand;         // candidates gathered from the boundary bin
+  uint32_t stotal, smax, sover;  // survivors, their largest key, a region overflowed
   uint64_t thr;           // the select's result
 };
 
@@ -404,8 +405,14 @@ __device__ uint32_t local_tau(const uint32_t* sample, int n, uint32_t q, uint32_
   }
   if (lane == 31) s.wscan[warp] = incl;
   __syncthreads();
-  uint32_t above = incl - sum;
-  for (int w = 0; w < warp; ++w) above += s.wscan[w];
+  const uint32_t wt = s.wscan[lane];
+  uint32_t wincl = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += v;
+  }
+  uint32_t above = __shfl_sync(0xffffffffu, wincl - wt, warp) + incl - sum;
   if (above < q && q <= above + sum) {
     for (int j = 0; j < kPer; ++j) {
       above += bins[top - j];
@@ -626,16 +633,25 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
       if constexpr (kCsize > 1) cg::this_cluster().sync();  // rank 1's survivors are in place
       else __syncthreads();
       if (rank == 0) {
-        uint32_t total = 0, cmax = 0;
-        bool over = false;
-#pragma unroll 8
-        for (int w = 0; w < kWarps; ++w) {
-          const uint32_t c = s.wsum[w] + s.wsum[kWarps + w];
-          total += c;
-          over |= c > static_cast<uint32_t>(kWarpCap);
-          cmax = max(cmax, s.wmax[w]);
-          if (csize > 1) cmax = max(cmax, s.wmax[kWarps + w]);
+        // one warp reduces the per-region counts and maxima (lane w: region w)
+        // and shares them: every thread walking all regions took ~4 k cycles
+        static_assert(kWarps == 32, "one lane per survivor region");
+        if (tid < 32) {
+          const uint32_t c = s.wsum[tid] + s.wsum[kWarps + tid];
+          uint32_t m = s.wmax[tid];
+          if (csize > 1) m = max(m, s.wmax[kWarps + tid]);
+          const uint32_t tot = __reduce_add_sync(0xffffffffu, c);
+          const uint32_t mx = __reduce_max_sync(0xffffffffu, m);
+          const bool ov = __any_sync(0xffffffffu, c > static_cast<uint32_t>(kWarpCap));
+          if (tid == 0) {
+            s.stotal = tot;
+            s.smax = mx;
+            s.sover = ov ? 1u : 0u;
+          }
         }
+        __syncthreads();
+        const uint32_t total = s.stotal, cmax = s.smax;
+        const bool over = s.sover != 0;
         if (!over && total >= static_cast<uint32_t>(p.k)) {
           const SrcPairs sp{s.data, s.data + kWarps * kWarpCap, s.wsum};
           static_assert(kBins % kT == 0 && kBins <= 2048, "hist holds kBins bins");
