@@ -36,6 +36,14 @@
 //              commit) and the ring slots.
 // With more than one split the pair writes unnormalised partial O plus its
 // (max, sum) and a combine kernel merges them.
+//
+// The gathers set the pace: one SM takes in ~20 B/cycle of scattered 128-byte
+// lines by 16-byte cp.async, whatever the number of gathering warps or ring
+// slots and whether the lines are in L2 or in HBM (measured on GB300), so a
+// tile costs the score CTA ~7.8 k cycles for its 144 KB of K-chunks.  Two S
+// tiles in TMEM, a third of the chunks by TMA tile::gather4, and an L2
+// prefetch of whole latent rows were each measured against this design and
+// did not beat it.
 #include <cuda_bf16.h>
 
 #include <cmath>
