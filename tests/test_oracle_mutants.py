@@ -5,8 +5,11 @@ exponent bias, a dropped scale or ReLU, a swapped nibble, a reversed operand,
 a wrong tie order, a value read from the wrong offset, a missing
 normalisation, ...), compiles the copy on the CPU, swaps it in for the real
 library, and runs every pin of tests/test_oracle_pins.py against it: at least
-one pin must fail.  The oracle itself is never modified.  Every planted slip
-keeps the copy's memory accesses inside the buffers the pins pass in."""
+one pin must fail.  The two schedule functions written in Python (the
+IndexCache / MLI layer sources and the prefill chunk plan) get the same
+treatment through patched copies of their source.  The oracle itself is never
+modified.  Every planted slip keeps the copy's memory accesses inside the
+buffers the pins pass in."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -132,6 +135,25 @@ def _failing_pins(golden_dir):
     return failed
 
 
+# Slips in the oracle's Python schedule functions: (function, old, new).
+PY_MUTANTS = {
+    "layer 0 attends nothing under MLI": ("layer_sources", "if mli and layer > 0:", "if mli:"),
+    "kept layers attend the previous one without MLI": (
+        "layer_sources", "out.append(layer if kept else latest)", "out.append(latest)"),
+    "every layer counts as an indexer layer": (
+        "layer_sources", "        if kept:\n            latest = layer", "        latest = layer"),
+    "chunk width not rounded to 4": (
+        "prefill_chunk_plan", "w = (max(int(c), int(min_cols)) + 3) // 4 * 4",
+        "w = max(int(c), int(min_cols))"),
+    "chunk width ignores min_cols": (
+        "prefill_chunk_plan", "w = (max(int(c), int(min_cols)) + 3) // 4 * 4",
+        "w = (int(c) + 3) // 4 * 4"),
+    "chunk budget exclusive": ("prefill_chunk_plan", "* 4 > budget_bytes:", "* 4 >= budget_bytes:"),
+    "new row's width left out of the budget": (
+        "prefill_chunk_plan", "(rows + 1) * max(width, w) * 4", "(rows + 1) * width * 4"),
+}
+
+
 def test_pins_pass_on_the_oracle(golden_dir):
     assert _failing_pins(golden_dir) == []
 
@@ -139,4 +161,15 @@ def test_pins_pass_on_the_oracle(golden_dir):
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_reject_planted_slip(name, mutant_libs, golden_dir, monkeypatch):
     monkeypatch.setattr(oracle, "_lib", ctypes.CDLL(mutant_libs[name]))
+    assert _failing_pins(golden_dir), f"no pin rejects the oracle with '{name}' planted"
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_pins_reject_planted_schedule_slip(name, golden_dir, monkeypatch):
+    fn_name, old, new = PY_MUTANTS[name]
+    src = inspect.getsource(getattr(oracle, fn_name))
+    assert src.count(old) == 1, (name, old)
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), oracle.__file__, "exec"), ns)
+    monkeypatch.setattr(oracle, fn_name, ns[fn_name])
     assert _failing_pins(golden_dir), f"no pin rejects the oracle with '{name}' planted"
