@@ -747,7 +747,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def main():
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -763,7 +763,11 @@ def main():
                     help="skip the multi-layer IndexCache / MLI schedule measurement")
     ap.add_argument("--no-candidate", action="store_true",
                     help="skip the candidate-path leg (profiling)")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = build_parser().parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
