@@ -344,6 +344,17 @@ def time_prefill(pst, steps, warmup, stream):
     return res, launches
 
 
+def kernel_roofline(alg_bytes, flops, ms, hbm_gbs, bf16_tflops):
+    """A kernel against its own roofline: the least time its algorithmic bytes
+    (at the measured copy bandwidth) and flops (at the bf16 tensor peak) allow,
+    divided by its measured time."""
+    t_mem = alg_bytes / (hbm_gbs * 1e9)
+    t_math = flops / (bf16_tflops * 1e12)
+    bound = t_mem if t_mem >= t_math else t_math
+    return {"bound": "hbm" if t_mem >= t_math else "tensor", "roofline_us": bound * 1e6,
+            "measured_us": ms * 1e3, "frac": bound / (ms * 1e-3)}
+
+
 def time_kernels(kernels, steps, warmup, stream):
     """Runs `steps` timed passes of the launches back to back (the step's time)
     and `steps` passes with an event after every launch (the per-kernel
@@ -607,11 +618,16 @@ def run_ours(args):
     traffic = INDEXER_DRAM_BYTES_PER_TOKEN * tokens
     t_idx = per["indexer"] * 1e-3
     achieved = alg_bytes / t_idx / 1e9
+    R = st["R"]
+    # top-k: 4 B per valid logit read + the indices written; sparse MLA: the
+    # selected latents (1152 B each) + Q read + O written, and its flops
+    topk_bytes = keys_per_step * 4 + R * TOPK * 4
+    mla_bytes = R * TOPK * 1152 + R * 128 * 576 * 2 + R * 128 * 512 * 2
+    mla_flops = R * 2 * 128 * TOPK * (576 + 512)
     e2e_serial_ms, h2d, d2h = e2e_decode(st, args.steps, args.warmup, stream)
     e2e_serial_ms = reduce_max(pg, e2e_serial_ms, device)
     e2e_ms = e2e_decode_pipelined(st, args.steps, args.warmup, stream)
     e2e_ms = reduce_max(pg, e2e_ms, device)
-    R = st["R"]
     # candidate path numbers
     cand = None
     if cst is not None:
@@ -681,10 +697,13 @@ def run_ours(args):
         "indexer": {"keys_per_s": keys_per_step / t_idx, "hbm_gbs": achieved,
                     "unique_keys_per_s": tokens / t_idx},
         "topk": {"rows_per_s": R / (per["topk"] * 1e-3),
-                 "logit_gbs": keys_per_step * 4 / (per["topk"] * 1e-3) / 1e9},
+                 "logit_gbs": keys_per_step * 4 / (per["topk"] * 1e-3) / 1e9,
+                 "roofline": kernel_roofline(topk_bytes, 0.0, per["topk"], hbm, bf16_tf)},
         "sparse_mla": {"attended_tok_per_s": R * TOPK / (per["sparse_mla"] * 1e-3),
                        "gather_gbs": R * TOPK * 1152 / (per["sparse_mla"] * 1e-3) / 1e9,
-                       "tflops": R * 2 * 128 * TOPK * (576 + 512) / (per["sparse_mla"] * 1e-3) / 1e12},
+                       "tflops": mla_flops / (per["sparse_mla"] * 1e-3) / 1e12,
+                       "roofline": kernel_roofline(mla_bytes, mla_flops, per["sparse_mla"], hbm,
+                                                   bf16_tf)},
         "candidate_path": cand,
         "layer_schedules": layers,
         "prefill_chunks": prefill,
