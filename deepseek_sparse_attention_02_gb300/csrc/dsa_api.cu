@@ -494,17 +494,15 @@ dsa_status dsa_sparse_mla_decode_static(const uint16_t* q, const uint16_t* kv_ca
   DeviceInfo dev;
   dsa_status st = device_ready(&dev);
   if (st != DSA_OK) return st;
-  MlaArgs a{q,   kv_cache, kv_page_stride, num_pages, block_table, bt_stride, num_req, next_n,
-            idx, k,        sm_scale,       out,       lse,         nullptr,   0};
-  size_t need = 0;
-  const cudaError_t e =
-      launch_sparse_mla_static(a, dev, static_cast<cudaStream_t>(stream), &need);
-  if (e == cudaErrorMemoryAllocation)
+  const size_t need = mla_workspace_size(static_cast<int>(R64), k);
+  if (need > mla_static_scratch_bytes())
     return fail(DSA_ERR_UNSUPPORTED,
                 "%s: this batch needs %zu bytes of split-K scratch but the static scratch holds "
                 "%zu; call dsa_sparse_mla_decode with a workspace instead",
                 fn, need, mla_static_scratch_bytes());
-  return cuda_status(e, fn);
+  MlaArgs a{q,   kv_cache, kv_page_stride, num_pages, block_table, bt_stride, num_req, next_n,
+            idx, k,        sm_scale,       out,       lse,         nullptr,   0};
+  return cuda_status(launch_sparse_mla_static(a, dev, static_cast<cudaStream_t>(stream)), fn);
 }
 
 }  // extern "C"

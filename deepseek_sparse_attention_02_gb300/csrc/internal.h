@@ -103,12 +103,10 @@ struct MlaArgs {
 size_t mla_workspace_size(int R, int k);
 cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
-// No-allocation variant: split-K scratch from a static device array.
-// Returns cudaErrorMemoryAllocation (and *need) when the batch needs more
-// scratch than the array holds.
+// No-allocation variant: split-K scratch from a static device array.  The
+// caller checks mla_workspace_size against mla_static_scratch_bytes first.
 size_t mla_static_scratch_bytes();
-cudaError_t launch_sparse_mla_static(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream,
-                                     size_t* need);
+cudaError_t launch_sparse_mla_static(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 struct CandExpandArgs {
   const int32_t* cand;  // [R, nb_cand] candidate block ids

@@ -416,7 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!bad && lane == 0) mbar_arrive(&s.q_ready);
     }
     // validity of a tile's 128 selections: lane j of every warp reads entries
-    // j, 32+j, 64+j, 96+j; four ballots give the tile's mask (read a tile ahead)
+    // j, 32+j, 64+j, 96+j; four ballots give the tile's mask.  A selection is
+    // valid if it is not -1 and its page is inside the cache: exactly the
+    // selections the gather warps copy (the others are zero-filled there and
+    // must get P = 0 here).  The indices are read two tiles ahead and their
+    // block-table entries one tile ahead.
     auto load_sel = [&](int i, int (&v)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -424,13 +428,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[u] = (i < ntile && pos < s1) ? idx_row[pos] : -1;
       }
     };
-    int sel[4];
-    load_sel(0, sel);
+    auto sel_ok = [&](const int (&v)[4], bool (&ok)[4]) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        ok[u] = false;
+        const int64_t pg_i = v[u] / 64;
+        if (v[u] >= 0 && req >= 0 && pg_i < p.bt_stride) {
+          const int pg = p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i];
+          ok[u] = pg >= 0 && pg < p.num_pages;
+        }
+      }
+    };
+    int sel_next[4];
+    bool ok_cur[4];
+    {
+      int sel0[4];
+      load_sel(0, sel0);
+      load_sel(1, sel_next);
+      sel_ok(sel0, ok_cur);
+    }
     for (int i = 0; i < ntile && !bad; ++i) {
       unsigned m[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) m[u] = __ballot_sync(0xffffffffu, sel[u] >= 0);
-      load_sel(i + 1, sel);
+      for (int u = 0; u < 4; ++u) m[u] = __ballot_sync(0xffffffffu, ok_cur[u]);
+      {
+        int sel_after[4];
+        load_sel(i + 2, sel_after);
+        sel_ok(sel_next, ok_cur);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sel_next[u] = sel_after[u];
+      }
       const bool all_valid = (m[0] & m[1] & m[2] & m[3]) == 0xffffffffu;  // warp-uniform
       const int b = i & 1;
       uint8_t* msg = msg0 + b * kMsgStride;
@@ -801,20 +828,18 @@ cudaError_t static_scratch_address(int device, void** out) {
 size_t mla_static_scratch_bytes() { return kStaticScratchBytes; }
 
 cudaError_t launch_sparse_mla_static(const MlaArgs& a_in, const DeviceInfo& dev,
-                                     cudaStream_t stream, size_t* need) {
+                                     cudaStream_t stream) {
+  // The address is looked up on every call's first use of a device, split or
+  // not, so a later call (perhaps under stream capture) makes no runtime query.
+  void* ptr = nullptr;
+  const cudaError_t e = static_scratch_address(dev.device, &ptr);
+  if (e != cudaSuccess) return e;
   const int R = a_in.row_bt ? a_in.rows : a_in.num_req * a_in.next_n;
-  *need = mla_workspace_size(R, a_in.k);
-  if (*need > kStaticScratchBytes) return cudaErrorMemoryAllocation;
+  const size_t need = mla_workspace_size(R, a_in.k);
+  if (need > kStaticScratchBytes) return cudaErrorInvalidValue;  // the caller checks first
   MlaArgs a = a_in;
-  a.ws = nullptr;
-  a.ws_bytes = 0;
-  if (*need > 0) {
-    void* ptr = nullptr;
-    const cudaError_t e = static_scratch_address(dev.device, &ptr);
-    if (e != cudaSuccess) return e;
-    a.ws = ptr;
-    a.ws_bytes = kStaticScratchBytes;
-  }
+  a.ws = need > 0 ? ptr : nullptr;
+  a.ws_bytes = need > 0 ? kStaticScratchBytes : 0;
   return launch_sparse_mla(a, dev, stream);
 }
 

@@ -73,6 +73,7 @@ EXPORTED = tuple(_SIGS)
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
           4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE"}
 DEVERR_TIMEOUT, DEVERR_BAD_PAGE, DEVERR_BAD_INDEX, DEVERR_CAPACITY = 1, 2, 4, 8
+DSA_MAX_TOPK = 8192  # include/dsa.h
 
 
 class DsaError(RuntimeError):

@@ -174,7 +174,10 @@ dsa_status dsa_topk_bf16(const uint16_t* logits, int64_t ld, const int32_t* row_
  *                         lse[r,g]   = log sum_j exp(z_j)           (natural log)
  *
  * over the valid selected tokens only (idx = -1 is skipped; a row with none
- * gives out = 0, lse = -inf).  Token positions are logical positions of the
+ * gives out = 0, lse = -inf).  An index whose page is outside the request's
+ * block-table row (idx / 64 >= bt_stride) or whose block-table entry is
+ * outside [0, num_pages) is skipped the same way and sets
+ * DSA_DEVERR_BAD_INDEX.  Token positions are logical positions of the
  * row's request (row r belongs to request r / next_n) and go through the block
  * table.  bf16 inputs, f32 accumulation and softmax, bf16 output.
  *
@@ -216,9 +219,9 @@ dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache,
  * (use dsa_sparse_mla_decode then).  Nothing is allocated, by this call or by
  * the library.
  *
- * The first call on a device looks up that device's scratch address
- * (cudaGetSymbolAddress, once per device, with the device current); make that
- * first call before any stream capture.  All calls on a device share the one
+ * The first call on a device, whatever its batch, looks up that device's
+ * scratch address (cudaGetSymbolAddress, once per device, with the device
+ * current); make that first call before any stream capture.  All calls on a device share the one
  * scratch array and it keeps the previous call's contents (no part of it has
  * to start at zero: each call writes every value it reads back); calls that
  * overlap on the GPU -- on two streams, or from two host threads -- race on

@@ -110,7 +110,8 @@ def decode_bf16(bits: np.ndarray) -> np.ndarray:
 
 
 def row_lengths(ctx_len: np.ndarray, next_n: int) -> np.ndarray:
-    """L_r for the flattened rows r = req*next_n + j (see the design doc readings)."""
+    """L_r for the flattened rows r = req*next_n + j: row j of a request sees
+    ctx_len - (next_n - 1 - j) tokens (its own position included)."""
     ctx = np.asarray(ctx_len, np.int64)
     j = np.arange(next_n, dtype=np.int64)
     L = ctx[:, None] - (next_n - 1 - j)[None, :]

@@ -39,6 +39,18 @@ def test_logits_judges_a_cancelled_sum_by_its_condition_scale():
         check_logits(np.array([[1e-9 + 6e-3, 2.0]]), ref, mag, [2])
 
 
+def test_logits_plain_mode_holds_the_stated_relative_bound_where_nothing_cancels():
+    # |ref| >= A/8: the plain 1e-3 relative error applies there; a cancelled
+    # sum (|ref| < A/8) is still judged by its condition scale only
+    ref = np.array([[2.0, 1e-6]])
+    mag = np.array([[8.0, 5.0]])
+    worst, plain = check_logits(np.array([[2.0 * (1 + 0.5e-3), 1e-6 + 4e-3]]), ref, mag, [2],
+                                plain=True)
+    assert 0.4e-3 < plain < 0.6e-3 and worst > 0.7e-3
+    with pytest.raises(AssertionError, match="plain relative"):
+        check_logits(np.array([[2.0 * (1 + 2e-3), 1e-6]]), ref, mag, [2], plain=True)
+
+
 def test_logits_rejects_non_finite_and_ignores_columns_past_the_row():
     ref, mag, L = _logit_case()
     got = ref.copy()

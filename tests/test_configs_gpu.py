@@ -43,7 +43,9 @@ def run_dense(cfg, with_mla):
     assert dsa.dsa_get_device_error() == 0
     rows = sample_rows(case.rows, seed=cfg)
     ref, mag = oracle_indexer(case, rows=rows, ld=ld)
-    check_logits(np_(logits)[rows], ref, mag, np_(L)[rows])
+    worst, worst_plain = check_logits(np_(logits)[rows], ref, mag, np_(L)[rows], plain=True)
+    print(f"config {cfg}: worst logit error {worst:.3g} of max(|ref|, A); "
+          f"plain relative error where |ref| >= A/8: {worst_plain:.3g}")
     check_topk_vs_oracle_scores(np_(sel)[rows], ref, mag, np_(L)[rows], K)
     exact_topk_all_rows(logits, L, sel)
     if with_mla:

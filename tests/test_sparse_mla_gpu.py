@@ -25,7 +25,8 @@ def run_case(ctx, next_n, k, seed, holes=0.0):
 
 def compare(mla, layout, next_n, idx, out, lse, rows=None, rel=0.0):
     """rel adds rel * |ref| to the absolute bound, element by element: the
-    output is stored in bf16, whose rounding alone is up to 2^-9 * |ref|."""
+    output is stored in bf16, whose rounding to nearest is up to half an ulp,
+    2^-8 * |ref| at worst (bf16 keeps 8 significant bits)."""
     o_ref, l_ref = mla_oracle(mla, layout.block_table, next_n, idx, rows=rows)
     got = np_(out.float())
     gl = np_(lse)

@@ -6,9 +6,12 @@ synchronisation an allocation may cause -- have no way to provide the split-K
 workspace of dsa_sparse_mla_decode.  This entry point keeps that scratch in
 an array compiled into the library.  The test calls it through the C ABI
 twice in a row (different inputs, so leftovers of the first call would show)
-and checks each result against dsa_sparse_mla_decode with a caller workspace,
-within the sparse-attention tolerance of the other parity tests.  It runs
-last (file name) and needs no state from other tests.
+and checks each result against dsa_sparse_mla_decode with a caller workspace:
+the two calls split the work the same way and run the same kernels, so out
+and lse must be bit for bit the same (a looser check, the sparse-attention
+tolerance of the other parity tests, is asserted first so a failure says how
+far apart they are).  It runs last (file name) and needs no state from other
+tests.
 """
 import pytest
 import torch
@@ -56,10 +59,15 @@ def test_static_scratch_matches_workspace_entry_point_twice():
         assert dsa.dsa_get_device_error() == 0
         assert (got_out.float() - ref_out.float()).abs().max().item() <= MLA_ATOL
         assert (got_lse - ref_lse).abs().max().item() <= LSE_ATOL
+        assert torch.equal(got_out.view(torch.int16), ref_out.view(torch.int16))
+        assert torch.equal(got_lse.view(torch.int32), ref_lse.view(torch.int32))
 
 
 def test_static_scratch_covers_every_batch_shape():
     from deepseek_sparse_attention_02_gb300 import dsa
-    # the largest split-K scratch any batch shape asks for fits the static array
-    worst = max(dsa.dsa_sparse_mla_workspace_size(R, 2048) for R in range(1, 200))
-    assert worst <= dsa.dsa_sparse_mla_static_scratch_bytes()
+    # the largest split-K scratch any batch shape asks for fits the static
+    # array, for selections from one token to the largest k
+    cap = dsa.dsa_sparse_mla_static_scratch_bytes()
+    for k in (1, 128, 2048, dsa.DSA_MAX_TOPK):
+        worst = max(dsa.dsa_sparse_mla_workspace_size(R, k) for R in range(1, 400))
+        assert worst <= cap, (k, worst, cap)
