@@ -228,7 +228,7 @@ def build_layers(st, n_layers=8):
                                            device=dev),
                            lse=torch.empty((R, W.MLA_HEADS), device=dev)))
     wsb = dsa.dsa_decode_layers_workspace_size(R, st["ld"], TOPK)
-    return dict(layers=layers, wsb=wsb, ws=torch.empty(wsb, dtype=torch.uint8, device=dev),
+    return dict(layers=layers, wsb=wsb, ws=torch.zeros(wsb, dtype=torch.uint8, device=dev),
                 side=torch.cuda.Stream(device=dev))
 
 
@@ -401,7 +401,7 @@ def e2e_decode_pipelined(st, steps, warmup, stream):
     case, mla, R, ld = st["case"], st["mla"], st["R"], st["ld"]
     c, lay = case.cache, case.layout
     host_in = [t.cpu().pin_memory() for t in (case.q, case.q_scale, case.w, lay.block_table,
-                                               lay.ctx_len, mla.q)]
+                                               lay.ctx_len, st["L"], mla.q)]
     sets = []
     for _ in range(2):
         ins = [torch.empty_like(t, device=st["out"].device) for t in host_in]
@@ -413,12 +413,12 @@ def e2e_decode_pipelined(st, steps, warmup, stream):
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
     def kernels(io):
-        q, qs, w, bt, ctx, mq = io["ins"]
+        q, qs, w, bt, ctx, rl, mq = io["ins"]
         out, lse, idx = io["outs"]
         dsa.dsa_indexer_logits(q, qs, w, c, W.FP8_PAGE_BYTES, c.data_ptr() + W.FP8_KEY_BYTES,
                                W.FP8_PAGE_BYTES, lay.num_pages, bt, ctx, len(lay.ctx_len), 2,
                                st["logits"], ld)
-        dsa.dsa_topk(st["logits"], ld, st["L"], R, TOPK, idx)
+        dsa.dsa_topk(st["logits"], ld, rl, R, TOPK, idx)
         dsa.dsa_sparse_mla_decode(mq, mla.kv, 64 * 576 * 2, lay.num_pages, bt, len(lay.ctx_len),
                                   2, idx, TOPK, mla.scale, out, lse, st["ws"], st["wsb"])
 
@@ -468,7 +468,7 @@ def e2e_decode(st, steps, warmup, stream):
     import torch
     case, mla = st["case"], st["mla"]
     dev_inputs = [case.q, case.q_scale, case.w, case.layout.block_table, case.layout.ctx_len,
-                  mla.q]
+                  st["L"], mla.q]
     host_inputs = [t.cpu().pin_memory() for t in dev_inputs]
     dev_outputs = [st["out"], st["lse"], st["idx"]]
     host_outputs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_outputs]

@@ -141,7 +141,7 @@ dsa_status indexer_impl(const char* fn, const uint8_t* q_fp8, const float* q_sca
                         const int32_t* block_table, int64_t bt_stride, const int32_t* ctx_len,
                         int num_req, int next_n, const int32_t* cu_rows, const int32_t* bt_rows,
                         int bt_num_rows, int total_rows, float* logits, int64_t ld,
-                        void* stream) {
+                        uint32_t* hist, void* stream) {
   if (!q_fp8 || !q_scale || !weights || !k_cache || !k_scale || !block_table || !ctx_len ||
       !logits)
     return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
@@ -171,6 +171,7 @@ dsa_status indexer_impl(const char* fn, const uint8_t* q_fp8, const float* q_sca
   a.bt_rows = bt_rows;
   a.total_rows = static_cast<int>(rows);
   a.bt_num_rows = bt_num_rows;
+  a.hist = hist;
   char msg[256] = "";
   cudaError_t e = launch_indexer(a, dev, static_cast<cudaStream_t>(stream), msg, sizeof(msg));
   if (e != cudaSuccess && msg[0]) return fail(DSA_ERR_UNSUPPORTED, "%s", msg);
@@ -180,7 +181,8 @@ dsa_status indexer_impl(const char* fn, const uint8_t* q_fp8, const float* q_sca
 // dsa_topk / dsa_topk_bf16: the checks and the launch, for f32 or bf16 scores.
 dsa_status topk_impl(const char* fn, const void* logits, bool bf16, int64_t ld,
                      const int32_t* row_len, int R, int k, const int32_t* col_blocks, int nb,
-                     int block_size, int32_t* out_idx, int force_path, void* stream) {
+                     int block_size, int32_t* out_idx, int force_path, uint32_t* hist,
+                     void* stream) {
   if (!logits || !row_len || !out_idx)
     return fail(DSA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
   if (R < 0 || k < 1 || k > DSA_MAX_TOPK || ld < 4 || ld % 4 || !aligned16(logits))
@@ -198,6 +200,7 @@ dsa_status topk_impl(const char* fn, const void* logits, bool bf16, int64_t ld,
   if (st != DSA_OK) return st;
   TopkArgs a{logits, ld, row_len, R, k, col_blocks, nb, block_size, out_idx, force_path,
              bf16 ? 1 : 0};
+  a.hist = hist;
   return cuda_status(launch_topk(a, dev, static_cast<cudaStream_t>(stream)), fn);
 }
 
@@ -255,7 +258,7 @@ using namespace dsa;
 
 extern "C" {
 
-int dsa_version(void) { return 100; }
+int dsa_version(void) { return 200; }
 
 const char* dsa_last_error(void) { return g_msg; }
 
@@ -285,7 +288,7 @@ dsa_status dsa_indexer_logits(const uint8_t* q_fp8, const float* q_scale, const 
                               int64_t ld, void* stream) {
   return dsa::indexer_impl("dsa_indexer_logits", q_fp8, q_scale, weights, k_cache, k_page_stride,
                            k_scale, s_page_stride, num_pages, block_table, bt_stride, ctx_len,
-                           num_req, next_n, nullptr, nullptr, 0, 0, logits, ld, stream);
+                           num_req, next_n, nullptr, nullptr, 0, 0, logits, ld, nullptr, stream);
 }
 
 dsa_status dsa_indexer_logits_varlen(const uint8_t* q_fp8, const float* q_scale,
@@ -308,21 +311,54 @@ dsa_status dsa_indexer_logits_varlen(const uint8_t* q_fp8, const float* q_scale,
   return dsa::indexer_impl(fn, q_fp8, q_scale, weights, k_cache, k_page_stride, k_scale,
                            s_page_stride, num_pages, block_table, bt_stride, ctx_len, num_entries,
                            max_rows, cu_rows, bt_rows, bt_num_rows, total_rows, logits, ld,
-                           stream);
+                           nullptr, stream);
 }
 
 dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
                     const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
                     int force_path, void* stream) {
   return dsa::topk_impl("dsa_topk", logits, false, ld, row_len, R, k, col_blocks, nb, block_size,
-                        out_idx, force_path, stream);
+                        out_idx, force_path, nullptr, stream);
 }
 
 dsa_status dsa_topk_bf16(const uint16_t* logits, int64_t ld, const int32_t* row_len, int R, int k,
                          const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
                          int force_path, void* stream) {
   return dsa::topk_impl("dsa_topk_bf16", logits, true, ld, row_len, R, k, col_blocks, nb,
-                        block_size, out_idx, force_path, stream);
+                        block_size, out_idx, force_path, nullptr, stream);
+}
+
+size_t dsa_score_hist_size(int R) {
+  if (R <= 0) return 0;
+  return static_cast<size_t>(R) * DSA_HIST_BINS * sizeof(uint32_t);
+}
+
+dsa_status dsa_indexer_logits_hist(const uint8_t* q_fp8, const float* q_scale,
+                                   const float* weights, const uint8_t* k_cache,
+                                   int64_t k_page_stride, const uint8_t* k_scale,
+                                   int64_t s_page_stride, int num_pages,
+                                   const int32_t* block_table, int64_t bt_stride,
+                                   const int32_t* ctx_len, int num_req, int next_n, float* logits,
+                                   int64_t ld, uint32_t* hist, void* stream) {
+  const char* fn = "dsa_indexer_logits_hist";
+  if (!hist || !aligned16(hist))
+    return fail(DSA_ERR_INVALID_ARG, "%s: hist must be a 16-byte aligned device buffer", fn);
+  if (next_n > 2)
+    return fail(DSA_ERR_UNSUPPORTED,
+                "%s: score histograms are built for decode (next_n <= 2), got next_n %d", fn,
+                next_n);
+  return dsa::indexer_impl(fn, q_fp8, q_scale, weights, k_cache, k_page_stride, k_scale,
+                           s_page_stride, num_pages, block_table, bt_stride, ctx_len, num_req,
+                           next_n, nullptr, nullptr, 0, 0, logits, ld, hist, stream);
+}
+
+dsa_status dsa_topk_hist(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
+                         uint32_t* hist, int32_t* out_idx, int force_path, void* stream) {
+  const char* fn = "dsa_topk_hist";
+  if (!hist || !aligned16(hist))
+    return fail(DSA_ERR_INVALID_ARG, "%s: hist must be a 16-byte aligned device buffer", fn);
+  return dsa::topk_impl(fn, logits, false, ld, row_len, R, k, nullptr, 0, 0, out_idx, force_path,
+                        hist, stream);
 }
 
 size_t dsa_sparse_mla_workspace_size(int R, int k) {

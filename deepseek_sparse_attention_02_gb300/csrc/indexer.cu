@@ -33,6 +33,13 @@
 // Decode (1-2 rows per group) is bound by the HBM read of the key cache
 // (132 B per token); a prefill chunk (4 rows per group, N = 256) is bound by
 // the tensor pipe and the epilogue ALU.
+//
+// With a histogram output (decode, at most 2 rows per group) the epilogue
+// also counts every logit it writes into a per-row histogram of its 12-bit
+// order-key prefix, in shared memory, and when the CTA leaves a row group it
+// adds the group's counts to the rows' histograms in global memory: the first
+// pass of the top-k (where its cutoff lies) done on the logits while they are
+// still in registers.
 #include <cstdio>
 
 #include "internal.h"
@@ -73,6 +80,7 @@ struct KParams {
   int bt_num_rows;          // with bt_rows: the rows of the block table
   float* logits;
   int64_t ld;
+  uint32_t* hist;           // null, or [rows, kHistBins] (zero on entry; counts are added)
   uint32_t* err;
 };
 
@@ -186,7 +194,7 @@ struct Cursor {
   }
 };
 
-template <int G>
+template <int G, bool kHist>
 struct Smem {
   static constexpr int N = 64 * G;
   static constexpr uint32_t kQBytes = N * 128;
@@ -202,9 +210,10 @@ struct Smem {
   uint32_t tmem_base;
   int abort;
   int scan_tmp[kThreads];
+  uint32_t hist[kHist ? G * kHistBins : 1];  // this CTA's counts for the current row group
 };
 
-template <int G>
+template <int G, bool kHist>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const KParams p) {
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kAcc % kMmaWarps == 0, "an accumulator must have a single MMA issuer");
   constexpr uint32_t kTmemCols = (kAcc * N <= 128) ? 128 : (kAcc * N <= 256 ? 256 : 512);
   constexpr uint32_t kIdesc = make_idesc(0, 0, 128, N, false, false);
-  using S = Smem<G>;
+  using S = Smem<G, kHist>;
   constexpr int kStages = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -237,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.prefix[0] = 0;
     s.abort = 0;
   }
+  if constexpr (kHist)
+    for (int i = tid; i < G * kHistBins; i += kThreads) s.hist[i] = 0;
   __syncthreads();
   {
     // Each thread sums a contiguous segment; one warp scans the partials.
@@ -431,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if constexpr (!kHist) {
     // ------------------------------------------------------------- epilogue --
     const int wg = (warp - kFirstEpiWarp) >> 2;  // which tiles (and accumulators) it drains
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
@@ -491,6 +502,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (left && lane == 0) mbar_arrive(&s.qempty[gslot]);
       __syncwarp();
     }
+  } else {
+    // ------------------------------------- epilogue with score histograms --
+    // A warp that has given up (a wait ran out) keeps walking the cursor
+    // without doing work, so that it still meets the other epilogue warps at
+    // every row-group barrier of the histogram flush.
+    const int wg = (warp - kFirstEpiWarp) >> 2;  // which tiles (and accumulators) it drains
+    const int quad = warp & 3;       // TMEM lane quadrant of this warp
+    const int row_in_tile = quad * 32 + lane;
+    const int etid = tid - 32 * kFirstEpiWarp;  // 0 .. 255
+    Cursor cur;
+    cur.init(s.prefix, p.ctx_len, p.cu_rows, p.total_rows, p.num_req, p.next_n, G, c0, c1);
+    int lt = 0;
+    bool bad = false;
+    while (cur.valid()) {
+      const int slot = cur.gcount & 1;
+      bool waited_q = false;
+      const int r0 = cur.row0();
+      const int nr = cur.nrows();
+      for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        if ((lt & 1) != wg || bad) continue;
+        if (!waited_q) {
+          if (!mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; continue; }
+          waited_q = true;
+        }
+        const int st = lt % kStages;
+        const int buf = lt % kAcc;
+        if (!mbar_wait_warp(&s.tfull[buf], (lt / kAcc) & 1, p.err, abort)) { bad = true; continue; }
+        tc_fence_after();
+        // the MMA has read the stage's keys (tfull); once every lane holds its
+        // scale the stage can be refilled
+        const float sc = s.scales[st][row_in_tile];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[st]);
+        const int tok = t * kTileTokens + row_in_tile;
+        const uint32_t taddr = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(buf * N);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float v[64];
+          tmem_ld64_sync(taddr + j * 64, v);
+          // four partial sums: a single 64-long FMA chain is latency bound
+          float a4[4] = {0.f, 0.f, 0.f, 0.f};
+          const float* wj = s.wq[slot] + j * 64;
+#pragma unroll
+          for (int h = 0; h < 64; ++h) a4[h & 3] = fmaf(wj[h], fmaxf(v[h], 0.f), a4[h & 3]);
+          const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+          if (j < nr && tok < cur.row_len(j) && tok < p.ld) {
+            const float logit = acc * sc;
+            p.logits[static_cast<int64_t>(r0 + j) * p.ld + tok] = logit;
+            atomicAdd(&s.hist[j * kHistBins + (order_key(logit) >> kHistShift)], 1u);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.tempty[buf]);
+      }
+      // A warp may walk through a group without processing any of its tiles (they
+      // went to the other warpgroup).  It still waits for that group's Q before it
+      // arrives on the slot's qempty, so its arrival cannot land in the phase of
+      // the group that used the slot two groups earlier.
+      if (!bad && !waited_q && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort))
+        bad = true;
+      const int gslot = slot;
+      const bool left = cur.next();
+      if (left && lane == 0 && !bad) mbar_arrive(&s.qempty[gslot]);
+      __syncwarp();
+      {
+        if (left) {
+          // both epilogue warpgroups are done with the group's tiles: add this
+          // CTA's counts to the rows' global histograms and clear them
+          const bool any_bad = named_bar_or(1, 256, bad);
+          if (!any_bad) {
+            for (int i = etid; i < nr * kHistBins; i += 256) {
+              const uint32_t c = s.hist[i];
+              if (c) {
+                atomicAdd(&p.hist[static_cast<int64_t>(r0 + (i >> kHistBits)) * kHistBins +
+                                  (i & (kHistBins - 1))],
+                          c);
+                s.hist[i] = 0;
+              }
+            }
+          }
+          named_bar_sync(1, 256);
+          bad = bad || any_bad;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -501,12 +599,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int G>
+template <int G, bool kHist>
 cudaError_t launch_g(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t stream,
                      const CUtensorMap& tk, const CUtensorMap& tq) {
-  static_assert(sizeof(Smem<G>) + 1024 <= 227 * 1024, "indexer shared memory exceeds 227 KB");
-  const size_t smem = sizeof(Smem<G>) + 1024;
-  auto fn = indexer_kernel<G>;
+  static_assert(sizeof(Smem<G, kHist>) + 1024 <= 227 * 1024, "indexer shared memory exceeds 227 KB");
+  const size_t smem = sizeof(Smem<G, kHist>) + 1024;
+  auto fn = indexer_kernel<G, kHist>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -527,6 +625,7 @@ cudaError_t launch_g(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t s
   p.bt_num_rows = a.bt_num_rows;
   p.logits = a.logits;
   p.ld = a.ld;
+  p.hist = a.hist;
   p.err = dev.err_word;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dev.sm_count);
@@ -570,11 +669,19 @@ cudaError_t launch_indexer(const IndexerArgs& a, const DeviceInfo& dev, cudaStre
                            msg_len))
       return cudaErrorInvalidValue;
   }
+  if (a.hist) {
+    if (G > 2) {
+      snprintf(msg, msg_len, "score histograms need at most 2 query rows per request (next_n %d)",
+               a.next_n);
+      return cudaErrorInvalidValue;
+    }
+    return G == 1 ? launch_g<1, true>(a, dev, stream, tk, tq) : launch_g<2, true>(a, dev, stream, tk, tq);
+  }
   switch (G) {
-    case 1: return launch_g<1>(a, dev, stream, tk, tq);
-    case 2: return launch_g<2>(a, dev, stream, tk, tq);
-    case 3: return launch_g<3>(a, dev, stream, tk, tq);
-    default: return launch_g<4>(a, dev, stream, tk, tq);
+    case 1: return launch_g<1, false>(a, dev, stream, tk, tq);
+    case 2: return launch_g<2, false>(a, dev, stream, tk, tq);
+    case 3: return launch_g<3, false>(a, dev, stream, tk, tq);
+    default: return launch_g<4, false>(a, dev, stream, tk, tq);
   }
 }
 

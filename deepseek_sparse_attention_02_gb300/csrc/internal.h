@@ -58,6 +58,7 @@ struct IndexerArgs {
   const int32_t* bt_rows = nullptr;  // varlen: block-table row of request i
   int total_rows = 0;                // varlen: cu_rows[num_req]
   int bt_num_rows = 0;               // varlen: rows of the block table
+  uint32_t* hist = nullptr;          // per-row score histograms [rows, 4096] (next_n <= 2)
 };
 
 cudaError_t launch_indexer(const IndexerArgs& a, const DeviceInfo& dev, cudaStream_t stream,
@@ -75,6 +76,7 @@ struct TopkArgs {
   int32_t* out;
   int force_path;
   int bf16;
+  uint32_t* hist = nullptr;  // per-row score histograms from the indexer; cleared on exit
 };
 
 cudaError_t launch_topk(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream);

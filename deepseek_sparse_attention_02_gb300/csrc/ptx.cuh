@@ -30,6 +30,19 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bit) {
 // at GB300 clocks).  A wait that runs out reports kErrTimeout and returns false.
 constexpr long long kWaitBudgetCycles = 2000000000LL;
 
+// Order-preserving u32 key of an f32 score: key(a) > key(b) iff a > b, with
+// -0.0 ranked as +0.0 (NaN unsupported).  Its top kHistBits bits (sign, 8
+// exponent bits, 3 mantissa bits) index the per-row score histogram the
+// indexer builds for the top-k: the bins are ordered like the scores.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u << 1) == 0) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;  // 4096 bins per row
+constexpr int kHistShift = 32 - kHistBits;
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

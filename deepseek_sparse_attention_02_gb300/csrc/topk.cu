@@ -18,8 +18,12 @@
 //  * staged path (rows shorter than 8k, up to kStage scores): the row's keys
 //    are staged in shared memory and the radix select runs over all of them;
 //  * cutoff path (longer rows; the "sampled filtering" of vLLM's persistent
-//    top-k in the RepoJournal digest): a sample of the row (runs of 8 scores
-//    spread over it) gives a cutoff tau expected to keep about 2k elements;
+//    top-k in the RepoJournal digest): the row's score histogram, when the
+//    indexer built one (12-bit order-key prefix, every logit counted), gives
+//    the exact cutoff at once: tau = the lower edge of the bin holding the
+//    k-th largest score, which keeps k + (that bin's count) at most;
+//    otherwise a sample of the row (runs of 8 scores spread over it) gives a
+//    cutoff tau expected to keep about 2k elements;
 //    one streaming pass compacts the survivors (key >= tau) into shared
 //    memory; the exact select then runs on the survivors only (its first
 //    digit linear in the key over [tau, largest survivor]).  If the
@@ -57,6 +61,7 @@ struct TkParams {
   int bs;
   int32_t* out;
   int force_path;
+  uint32_t* hist;  // null, or [R, kHistBins] score histograms; every row's is cleared
   uint32_t* err;
 };
 
@@ -74,11 +79,7 @@ struct TkSmem {
   uint64_t thr;           // the select's result
 };
 
-__device__ __forceinline__ uint32_t key_of(float x) {
-  uint32_t u = __float_as_uint(x);
-  if ((u << 1) == 0) u = 0;  // -0.0 ranks with +0.0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+__device__ __forceinline__ uint32_t key_of(float x) { return order_key(x); }
 
 // Radix state: the selected set is every element whose top kb bits of key and
 // (once kb == 32) top ib bits of ~column are >= (phi, plo).  Digits are up to
@@ -428,6 +429,61 @@ __device__ uint32_t local_tau(const uint32_t* sample, int n, uint32_t q, uint32_
   return tau;
 }
 
+// Cutoff from the row's score histogram h (kHistBins counts of the 12-bit
+// key prefix, bin b = keys [b << kHistShift, (b + 1) << kHistShift)): the
+// lower edge of the bin holding the k-th largest score, so that every score
+// of the higher bins (fewer than k) and the whole boundary bin survive.
+// Thread t scans bins [kHistBins - 4(t+1), kHistBins - 4t) downwards.  Returns
+// false when the histogram does not count exactly L scores (it was not built
+// for this row): the caller then estimates the cutoff from a sample.
+__device__ bool hist_tau(const uint32_t* h, int L, uint32_t k, TkSmem& s, uint32_t* tau) {
+  constexpr int kPer = kHistBins / kT;
+  static_assert(kPer == 4, "one 16-byte load of bins per thread");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int top = kHistBins - kPer * tid - 1;
+  // plain (coherent) load: this kernel clears the histogram after reading it
+  const uint4 v = *reinterpret_cast<const uint4*>(h + top - 3);
+  const uint32_t hh[4] = {v.w, v.z, v.y, v.x};  // bins top, top-1, top-2, top-3
+  const uint32_t sum = (hh[0] + hh[1]) + (hh[2] + hh[3]);
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s.wscan[warp] = incl;
+  __syncthreads();
+  const uint32_t wt = s.wscan[lane];
+  uint32_t wincl = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += t;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, wincl, 31);
+  uint32_t above = __shfl_sync(0xffffffffu, wincl - wt, warp) + incl - sum;
+  if (above < k && k <= above + sum) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (above + hh[j] >= k) {
+        s.bin = static_cast<uint32_t>(top - j);
+        break;
+      }
+      above += hh[j];
+    }
+  }
+  __syncthreads();
+  *tau = s.bin << kHistShift;
+  __syncthreads();
+  return total == static_cast<uint32_t>(L);
+}
+
+// Clears a row's histogram (all threads of one CTA).
+__device__ __forceinline__ void clear_hist(uint32_t* h) {
+  static_assert(kHistBins == 4 * kT, "one 16-byte store per thread");
+  reinterpret_cast<uint4*>(h)[threadIdx.x] = make_uint4(0, 0, 0, 0);
+}
+
 // One streaming pass over the columns [col0, col0 + g.n) of the row (g.row
 // points at column col0): every element with key >= tau goes to its warp's
 // region of (keys, cols), [w*kWarpCap, (w+1)*kWarpCap), filled from the bottom
@@ -568,11 +624,14 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
       L = static_cast<int>(p.ld);
     }
     int32_t* out = p.out + static_cast<int64_t>(row) * p.k;
+    uint32_t* const hrow = p.hist ? p.hist + static_cast<int64_t>(row) * kHistBins : nullptr;
 
     if (L <= p.k) {
       // every column is selected; the tail is -1
-      if (rank == 0)
+      if (rank == 0) {
         for (int c = tid; c < p.k; c += kT) out[c] = c < L ? map_col(p, row, c) : -1;
+        if (hrow) clear_hist(hrow);
+      }
       continue;
     }
 
@@ -586,30 +645,35 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
         (p.force_path == 0 && (L > kStage || static_cast<int64_t>(L) >= 8ll * p.k));
     bool done = false;
     if (cutoff) {
-      // 1. the row's sample -> cutoff tau expected to keep about 2k elements.
-      // Rows shorter than the sample are taken whole.
-      int ns;
-      if (L >= kSample) {
-        ns = kSample;
-        if (tid < kSample / 4) {
-          // float4 tid of the sample: group tid / 2, half tid % 2
-          const int64_t g0 =
-              ((static_cast<int64_t>(tid >> 1) * (L - 8)) / (kGroups - 1)) & ~3ll;
-          const float4 v = rowp.load4(g0 + 4 * (tid & 1));
-          *reinterpret_cast<uint4*>(s.sample + 4 * tid) =
-              make_uint4(key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w));
+      // 1. the cutoff tau: exact from the row's histogram, or from a sample
+      // (expected to keep about 2k elements; rows shorter than the sample are
+      // taken whole)
+      uint32_t tau = 0;
+      const bool exact = hrow && hist_tau(hrow, L, static_cast<uint32_t>(p.k), s, &tau);
+      if (!exact) {
+        int ns;
+        if (L >= kSample) {
+          ns = kSample;
+          if (tid < kSample / 4) {
+            // float4 tid of the sample: group tid / 2, half tid % 2
+            const int64_t g0 =
+                ((static_cast<int64_t>(tid >> 1) * (L - 8)) / (kGroups - 1)) & ~3ll;
+            const float4 v = rowp.load4(g0 + 4 * (tid & 1));
+            *reinterpret_cast<uint4*>(s.sample + 4 * tid) =
+                make_uint4(key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w));
+          }
+        } else {
+          ns = L;
+          for (int i = tid; i < L; i += kT) s.sample[i] = key_of(rowp.load1(i));
         }
-      } else {
-        ns = L;
-        for (int i = tid; i < L; i += kT) s.sample[i] = key_of(rowp.load1(i));
+        __syncthreads();
+        // q = ceil(2k ns / L) sample keys above tau (integer arithmetic: FP64 is
+        // a slow pipe on GB300 and every thread evaluates this)
+        const int64_t want = (2 * static_cast<int64_t>(p.k) * ns + L - 1) / L;
+        const uint32_t q = static_cast<uint32_t>(want < ns ? want : ns);
+        // the survivor area is free until the compaction: it holds the bins
+        tau = local_tau(s.sample, ns, q > 0 ? q : 1u, s.data, s);
       }
-      __syncthreads();
-      // q = ceil(2k ns / L) sample keys above tau (integer arithmetic: FP64 is
-      // a slow pipe on GB300 and every thread evaluates this)
-      const int64_t want = (2 * static_cast<int64_t>(p.k) * ns + L - 1) / L;
-      const uint32_t q = static_cast<uint32_t>(want < ns ? want : ns);
-      // the survivor area is free until the compaction: it holds the bins
-      const uint32_t tau = local_tau(s.sample, ns, q > 0 ? q : 1u, s.data, s);
       // 2. one streaming pass: compact the survivors (key >= tau); with two
       // CTAs, columns [0, h) and [h, L), h a multiple of 4 (16-byte loads)
       const int h = csize > 1 ? ((L + 7) >> 3) << 2 : L;
@@ -688,6 +752,9 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
     }
     __syncthreads();  // all emits done before the counter and the buffers are reused
     if constexpr (kCsize > 1) cg::this_cluster().sync();  // rank 0 is done with the regions rank 1 refills
+    // both CTAs read the histogram before the syncs above: clear it for the
+    // next use
+    if (rank == 0 && hrow) clear_hist(hrow);
   }
 }
 
@@ -698,8 +765,8 @@ namespace {
 template <class T>
 cudaError_t launch_topk_t(const TopkArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   const size_t smem = sizeof(TkSmem) + 16;
-  TkParams p{a.logits, a.ld,  a.row_len, a.R,          a.k,          a.col_blocks,
-             a.nb,     a.block_size, a.out, a.force_path, dev.err_word};
+  TkParams p{a.logits, a.ld,         a.row_len, a.R,          a.k,    a.col_blocks,
+             a.nb,     a.block_size, a.out,     a.force_path, a.hist, dev.err_word};
   // Two CTAs per row while that leaves no row waiting for an SM and the rows
   // can be long enough for the halved streaming pass to repay the cluster's
   // costs: measured at 64 rows, k = 2048, the pair is ~2 us slower at 65536

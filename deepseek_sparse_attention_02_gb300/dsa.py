@@ -39,6 +39,10 @@ _SIGS = {
     "dsa_indexer_logits": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _P, _I, _I, _P, _I64,
                             _P], _I),
     "dsa_topk": ([_P, _I64, _P, _I, _I, _P, _I, _I, _P, _I, _P], _I),
+    "dsa_score_hist_size": ([_I], _SZ),
+    "dsa_indexer_logits_hist": ([_P, _P, _P, _P, _I64, _P, _I64, _I, _P, _I64, _P, _I, _I, _P,
+                                 _I64, _P, _P], _I),
+    "dsa_topk_hist": ([_P, _I64, _P, _I, _I, _P, _P, _I, _P], _I),
     "dsa_sparse_mla_workspace_size": ([_I, _I], _SZ),
     "dsa_sparse_mla_decode": ([_P, _P, _I64, _I, _P, _I64, _I, _I, _P, _I, _F, _P, _P, _P, _SZ,
                                _P], _I),
@@ -74,6 +78,7 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
           4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE"}
 DEVERR_TIMEOUT, DEVERR_BAD_PAGE, DEVERR_BAD_INDEX, DEVERR_CAPACITY = 1, 2, 4, 8
 DSA_MAX_TOPK = 8192  # include/dsa.h
+DSA_HIST_BINS = 4096
 
 
 class DsaError(RuntimeError):
@@ -139,6 +144,27 @@ def dsa_topk(logits, ld, row_len, R, k, out_idx, col_blocks=None, nb=0, block_si
              force_path=0, stream=None):
     _check(_lib.dsa_topk(_ptr(logits), ld, _ptr(row_len), R, k, _ptr(col_blocks), nb, block_size,
                          _ptr(out_idx), force_path, _stream(stream)))
+
+
+def dsa_score_hist_size(R: int) -> int:
+    return _lib.dsa_score_hist_size(R)
+
+
+def dsa_indexer_logits_hist(q_fp8, q_scale, weights, k_cache, k_page_stride, k_scale,
+                            s_page_stride, num_pages, block_table, ctx_len, num_req, next_n, logits,
+                            ld, hist, stream=None):
+    """dsa_indexer_logits that also adds per-row score histograms into hist."""
+    bt_stride = block_table.shape[1]
+    _check(_lib.dsa_indexer_logits_hist(_ptr(q_fp8), _ptr(q_scale), _ptr(weights), _ptr(k_cache),
+                                        k_page_stride, _ptr(k_scale), s_page_stride, num_pages,
+                                        _ptr(block_table), bt_stride, _ptr(ctx_len), num_req,
+                                        next_n, _ptr(logits), ld, _ptr(hist), _stream(stream)))
+
+
+def dsa_topk_hist(logits, ld, row_len, R, k, hist, out_idx, force_path=0, stream=None):
+    """dsa_topk placing its cutoff from the histograms (and clearing them)."""
+    _check(_lib.dsa_topk_hist(_ptr(logits), ld, _ptr(row_len), R, k, _ptr(hist), _ptr(out_idx),
+                              force_path, _stream(stream)))
 
 
 def dsa_topk_bf16(logits, ld, row_len, R, k, out_idx, col_blocks=None, nb=0, block_size=0,

@@ -81,6 +81,7 @@ typedef enum {
 #define DSA_MLA_DQK 576 /* 512 latent + 64 rope */
 #define DSA_MLA_DV 512
 #define DSA_MAX_TOPK 8192
+#define DSA_HIST_BINS 4096 /* bins of a row's score histogram (dsa_indexer_logits_hist) */
 
 /* Version of this ABI (major*100 + minor). */
 int dsa_version(void);
@@ -156,6 +157,43 @@ dsa_status dsa_indexer_logits(const uint8_t* q_fp8, const float* q_scale, const 
 dsa_status dsa_topk(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
                     const int32_t* col_blocks, int nb, int block_size, int32_t* out_idx,
                     int force_path, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_indexer_logits_hist + dsa_topk_hist -- the indexer and the top-k with
+ * the top-k's first pass fused into the indexer's epilogue.
+ *
+ * dsa_indexer_logits_hist is dsa_indexer_logits that also counts every logit
+ * it writes into a per-row histogram: hist[r, b] += #{t < L_r : the top 12
+ * bits of key(logits[r, t]) == b}, where key is the order-preserving u32 of
+ * the f32 (sign bit flipped for positives, all bits for negatives; -0.0 as
+ * +0.0), so bin b holds the scores of one sign, exponent and 3 leading
+ * mantissa bits, and the bins are ordered like the scores.  Decode only:
+ * next_n <= 2, else DSA_ERR_UNSUPPORTED.
+ * dsa_topk_hist is dsa_topk (no column map) that reads row r's histogram to
+ * place its cutoff at once (the lower edge of the bin holding the k-th
+ * largest score) instead of estimating it from a sample, and clears every
+ * row's histogram to zero before it returns.
+ *
+ *   hist   device [R, DSA_HIST_BINS] uint32 (dsa_score_hist_size(R) bytes),
+ *          16-byte aligned.  Zero-fill it once after allocating it; each
+ *          dsa_indexer_logits_hist adds its counts and the dsa_topk_hist that
+ *          follows leaves it zero again.  The result never depends on the
+ *          histogram: one that does not count exactly row_len[r] scores is
+ *          ignored (the sample estimate is used), and a cutoff that keeps
+ *          fewer than k scores or more than fit is redone exactly.
+ * ---------------------------------------------------------------------- */
+size_t dsa_score_hist_size(int R);
+
+dsa_status dsa_indexer_logits_hist(const uint8_t* q_fp8, const float* q_scale,
+                                   const float* weights, const uint8_t* k_cache,
+                                   int64_t k_page_stride, const uint8_t* k_scale,
+                                   int64_t s_page_stride, int num_pages,
+                                   const int32_t* block_table, int64_t bt_stride,
+                                   const int32_t* ctx_len, int num_req, int next_n, float* logits,
+                                   int64_t ld, uint32_t* hist, void* stream);
+
+dsa_status dsa_topk_hist(const float* logits, int64_t ld, const int32_t* row_len, int R, int k,
+                         uint32_t* hist, int32_t* out_idx, int force_path, void* stream);
 
 /* dsa_topk over bf16 scores (the vLLM sparse_indexer page's pairing: bf16
  * sparse logits selected by a bf16 top-k).  Same arguments and result; each

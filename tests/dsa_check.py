@@ -20,6 +20,7 @@ import oracle
 from deepseek_sparse_attention_02_gb300 import workloads as W
 
 LOGIT_RTOL = 1e-3
+HIST_BINS = 4096
 MLA_ATOL = 1e-2
 LSE_ATOL = 1e-3
 
@@ -136,3 +137,15 @@ def gpu_mla(mla, bt, num_req, next_n, idx, num_pages):
     dsa.dsa_sparse_mla_decode(mla.q, mla.kv, 64 * 576 * 2, num_pages, bt, num_req, next_n, idx, k,
                               mla.scale, out, lse, ws, wsb)
     return out, lse
+
+
+def host_hist(logits, L):
+    """[R, 4096] counts of the 12-bit order-key prefix of logits[r, :L[r]]."""
+    out = np.zeros((len(L), HIST_BINS), np.int64)
+    for r, n in enumerate(L):
+        u = np.ascontiguousarray(logits[r, :int(n)], dtype=np.float32).view(np.uint32).copy()
+        u[(u << np.uint32(1)) == 0] = 0                       # -0.0 ranks as +0.0
+        neg = (u & np.uint32(0x80000000)) != 0
+        key = np.where(neg, ~u, u | np.uint32(0x80000000))
+        out[r] = np.bincount((key >> np.uint32(20)).astype(np.int64), minlength=HIST_BINS)
+    return out

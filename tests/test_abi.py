@@ -35,7 +35,9 @@ def test_every_declared_symbol_is_exported(dsa):
 
 
 def test_version_and_sizes(dsa):
-    assert dsa.dsa_version() == 100
+    assert dsa.dsa_version() == 200
+    assert dsa.dsa_score_hist_size(64) == 64 * 4096 * 4
+    assert dsa.dsa_score_hist_size(0) == 0
     assert dsa.dsa_sparse_mla_workspace_size(64, 2048) == 0          # one wave, no split
     assert dsa.dsa_sparse_mla_workspace_size(1, 2048) > 0            # split-K partials
     assert dsa.dsa_candidate_schedule_size(64) >= 65 * 4
@@ -60,3 +62,14 @@ def test_host_validation_without_gpu(dsa):
     # an empty batch is a no-op that needs no device
     assert lib.dsa_indexer_logits(16, 16, 16, 16, 8448, 16, 8448, 1, 16, 1, 16, 0, 1, 16, 4,
                                   None) == 0
+
+    # fused-histogram pair: hist is required and 16-byte aligned; the indexer
+    # builds histograms for decode shapes only (next_n <= 2)
+    assert lib.dsa_topk_hist(16, 2048, 16, 1, 8, None, 16, 0, None) == 1
+    assert lib.dsa_topk_hist(16, 2048, 16, 1, 8, 20, 16, 0, None) == 1
+    assert lib.dsa_indexer_logits_hist(16, 16, 16, 16, 8448, 16, 8448, 1, 16, 1, 16, 1, 1, 16, 4,
+                                       None, None) == 1
+    assert lib.dsa_indexer_logits_hist(16, 16, 16, 16, 8448, 16, 8448, 1, 16, 1, 16, 1, 3, 16, 4,
+                                       16, None) == 2
+    assert lib.dsa_indexer_logits_hist(16, 16, 16, 16, 8448, 16, 8448, 1, 16, 1, 16, 0, 2, 16, 4,
+                                       16, None) == 0

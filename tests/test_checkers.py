@@ -5,7 +5,7 @@ from __future__ import annotations
 import numpy as np
 import pytest
 
-from dsa_check import LOGIT_RTOL, check_logits, check_topk_vs_oracle_scores
+from dsa_check import LOGIT_RTOL, check_logits, check_topk_vs_oracle_scores, host_hist
 
 
 def _logit_case(seed=0, n=200):
@@ -101,3 +101,20 @@ def test_topk_short_rows_need_every_token_then_padding():
         check_topk_vs_oracle_scores(np.array([[4, 0, 2, 1, 3, 0, -1, -1]]), ref, mag, [5], 8)
     with pytest.raises(AssertionError):
         check_topk_vs_oracle_scores(np.array([[4, 0, 2, 1, -1, -1, -1, -1]]), ref, mag, [5], 8)
+
+
+def test_host_histogram_bins_follow_the_score_order():
+    # the reference histogram of the indexer's fused top-k pass: bins ordered
+    # like the scores, -0.0 with +0.0, 1.0 in bin 0xBF8 (sign flipped:
+    # 0xBF800000 >> 20), -1.0 in bin 0x407 (all bits flipped: 0x407FFFFF >> 20)
+    vals = np.array([-np.inf, -3e38, -2.0, -1.0, -1e-30, -0.0, 0.0, 1e-30, 1.0, 1.0625, 2.0,
+                     3e38, np.inf], np.float32)
+    bins = [int(np.argmax(host_hist(np.array([[v]], np.float32), [1])[0])) for v in vals]
+    assert bins == sorted(bins)
+    assert bins[5] == bins[6] == 0x800
+    assert bins[8] == 0xBF8 and bins[3] == 0x407
+    assert bins[9] == bins[8]  # 1.0625 shares 1.0's three leading mantissa bits
+    rng = np.random.default_rng(0)
+    x = rng.normal(size=(3, 5000)).astype(np.float32) * 10
+    h = host_hist(x, [5000, 4000, 10])
+    assert h.sum(axis=1).tolist() == [5000, 4000, 10]
