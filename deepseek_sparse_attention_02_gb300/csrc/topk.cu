@@ -68,6 +68,8 @@ struct TkParams {
 struct TkSmem {
   uint32_t data[kStage];  // staged keys | survivor keys (warp regions) + columns
   uint32_t sample[kSample];
+  uint32_t tau_bins[4096];  // the cutoff estimate's histogram (its own: the second CTA of a
+                            // pair may already be writing survivors into rank 0's data)
   uint32_t hist[2048];    // radix histogram (kBins)
   uint32_t wscan[kWarps]; // per-warp scan totals
   uint32_t wsum[2 * kWarps];  // per-region survivor counts (a region per warp of the row's CTAs)
@@ -671,8 +673,7 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
         // a slow pipe on GB300 and every thread evaluates this)
         const int64_t want = (2 * static_cast<int64_t>(p.k) * ns + L - 1) / L;
         const uint32_t q = static_cast<uint32_t>(want < ns ? want : ns);
-        // the survivor area is free until the compaction: it holds the bins
-        tau = local_tau(s.sample, ns, q > 0 ? q : 1u, s.data, s);
+        tau = local_tau(s.sample, ns, q > 0 ? q : 1u, s.tau_bins, s);
       }
       // 2. one streaming pass: compact the survivors (key >= tau); with two
       // CTAs, columns [0, h) and [h, L), h a multiple of 4 (16-byte loads)
