@@ -16,8 +16,14 @@ All inputs are seeded synthetic data generated on the device; the key cache
 (553.6 MB) and the latent cache (4.8 GB) are larger than L2, so no flush is
 needed between steps.
 
---impl reference times the fp64 CPU oracle (the reference arm) on bounded
-samples of the same workload.
+The tiny decode (1 x 8192 tokens) and the batched varlen full path (64
+requests, L ~ U[16K, 64K], indexer + top-2048 + sparse MLA) are timed in the
+same run ("configs"), and the chunked prefill's launches are broken down with
+their tensor-pipe fractions.  The fp64 CPU oracle is timed on the host cores on
+every workload ("cpu_baseline").
+
+--impl reference times the fp64 CPU oracle (the reference arm) on the
+headline workload's 64 rows per step.
 """
 from __future__ import annotations
 
@@ -48,12 +54,22 @@ TOPK = 2048
 
 
 def peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s burst, source): the copy bandwidth and the
+    cuBLAS bf16 rate measured on this machine; each kernel here is timed alone
+    (one launch between two events), so its tensor peak is the burst figure.
+    FP8 kind::f8f6f4 contractions take twice the bf16 figure (the nominal
+    dense ratio, 4.5 / 2.25 PFLOP/s)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops_sustained"]), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     except Exception:
-        return 6800.0, 1700.0, "fallback"
+        return 6800.0, 1900.0, "fallback"
+
+
+# Targets the method's statement sets for one GB300: the 128K decode indexer at
+# >= 70 % of the HBM roofline, the top-k and the sparse MLA >= 50 % of theirs.
+TARGETS = {"indexer_hbm_frac": 0.70, "topk_frac": 0.50, "sparse_mla_frac": 0.50}
 
 
 class ClockSampler:
@@ -157,6 +173,79 @@ def decode_kernels(st):
                                   st["lse"], st["ws"], st["wsb"])
 
     return [("indexer", indexer), ("topk", topk), ("sparse_mla", mla)]
+
+
+def build_dense_config(device, cfg):
+    """The tiny decode (cfg 0: 1 request x 8192 tokens, contiguous cache,
+    indexer + top-2048) or the batched varlen full path (cfg 1: 64 requests,
+    L ~ U[16K, 64K], shuffled pages, indexer + top-2048 + sparse MLA)."""
+    import torch
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    spec = W.config_ctx(cfg)
+    case = W.make_indexer_case(spec["ctx"], next_n=spec["next_n"], seed=cfg, device=device,
+                               shuffle=spec["shuffle"])
+    R = case.rows
+    L = W.row_lengths(case.layout.ctx_len, spec["next_n"]).to(torch.int32)
+    ld = (int(L.max()) + 3) // 4 * 4
+    st = dict(cfg=cfg, case=case, R=R, L=L, ld=ld, next_n=spec["next_n"],
+              logits=torch.empty((R, ld), device=device),
+              idx=torch.empty((R, TOPK), dtype=torch.int32, device=device), mla=None)
+    if cfg == 1:
+        st["mla"] = W.make_mla_case(R, case.layout.num_pages, seed=cfg, device=device)
+        st["out"] = torch.empty((R, W.MLA_HEADS, W.MLA_DV), dtype=torch.bfloat16, device=device)
+        st["lse"] = torch.empty((R, W.MLA_HEADS), device=device)
+        st["wsb"] = dsa.dsa_sparse_mla_workspace_size(R, TOPK)
+        st["ws"] = torch.empty(max(st["wsb"], 16), dtype=torch.uint8, device=device)
+    return st
+
+
+def dense_config_kernels(st):
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case, R, ld, nn = st["case"], st["R"], st["ld"], st["next_n"]
+    c, lay = case.cache, case.layout
+
+    def indexer():
+        dsa.dsa_indexer_logits(case.q, case.q_scale, case.w, c, W.FP8_PAGE_BYTES,
+                               c.data_ptr() + W.FP8_KEY_BYTES, W.FP8_PAGE_BYTES, lay.num_pages,
+                               lay.block_table, lay.ctx_len, len(lay.ctx_len), nn, st["logits"], ld)
+
+    def topk():
+        dsa.dsa_topk(st["logits"], ld, st["L"], R, TOPK, st["idx"])
+    ks = [("indexer", indexer), ("topk", topk)]
+    if st["mla"] is not None:
+        def mla():
+            m = st["mla"]
+            dsa.dsa_sparse_mla_decode(m.q, m.kv, 64 * 576 * 2, lay.num_pages, lay.block_table,
+                                      len(lay.ctx_len), nn, st["idx"], TOPK, m.scale, st["out"],
+                                      st["lse"], st["ws"], st["wsb"])
+        ks.append(("sparse_mla", mla))
+    return ks
+
+
+def dense_metrics(st, total_ms, per, steps, hbm, bf16_tf):
+    """Throughput and per-kernel roofline fractions of a dense decode leg."""
+    R = st["R"]
+    keys = float(st["L"].sum().item())
+    tokens = float(st["case"].layout.ctx_len.sum().item())
+    ms = total_ms / steps
+    idx_bytes = tokens * 132 + keys * 4
+    out = {"ms_per_step": round(ms, 4),
+           "breakdown_ms": {k: round(v, 4) for k, v in per.items()},
+           "keys_per_s": keys / (ms * 1e-3),
+           "indexer_keys_per_s": keys / (per["indexer"] * 1e-3),
+           "indexer_hbm_frac": round(idx_bytes / (per["indexer"] * 1e-3) / 1e9 / hbm, 4),
+           "topk_rows_per_s": R / (per["topk"] * 1e-3),
+           "topk_frac": round(kernel_roofline(keys * 4 + R * TOPK * 4, 0.0, per["topk"], hbm,
+                                              bf16_tf)["frac"], 4)}
+    if "sparse_mla" in per:
+        mla_bytes = R * TOPK * 1152 + R * 128 * 576 * 2 + R * 128 * 512 * 2
+        mla_flops = R * 2 * 128 * TOPK * (576 + 512)
+        out["attended_tok_per_s"] = R * TOPK / (per["sparse_mla"] * 1e-3)
+        out["sparse_mla_frac"] = round(kernel_roofline(mla_bytes, mla_flops, per["sparse_mla"],
+                                                       hbm, bf16_tf)["frac"], 4)
+    return out
 
 
 def build_candidate(device, seed=3):
@@ -325,6 +414,47 @@ def prefill_step(pst, plan):
                                          P["ws"], P["wsb"])
         launches += 5 + (1 if wsb > 0 else 0)
     return launches
+
+
+def prefill_kernel_ms(pst, plan, reps, stream):
+    """Mean ms per step of the prefill's indexer, top-k and sparse MLA launches
+    (events around each launch of every chunk, summed over the chunks)."""
+    import torch
+    from deepseek_sparse_attention_02_gb300 import dsa
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case, mla = pst["case"], pst["mla"]
+    lay, c = case.layout, case.cache
+    P = pst["plans"][plan]
+    acc = {"indexer": 0.0, "topk": 0.0, "sparse_mla": 0.0}
+    for _ in range(reps):
+        evs = []
+        for ch in P["chunks"]:
+            j0, n, ld = ch["j0"], ch["n"], ch["ld"]
+            logits = P["logits"][:n]
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            dsa.dsa_indexer_logits_varlen(case.q[j0:j0 + n], case.q_scale[j0:j0 + n],
+                                          case.w[j0:j0 + n], c, W.FP8_PAGE_BYTES,
+                                          c.data_ptr() + W.FP8_KEY_BYTES, W.FP8_PAGE_BYTES,
+                                          lay.num_pages, lay.block_table, ch["btr"], ch["ctx"],
+                                          ch["cu"], 1, n, n, logits, ld)
+            e[1].record(stream)
+            dsa.dsa_varlen_row_lengths(ch["ctx"], ch["cu"], 1, n, P["row_len"])
+            dsa.dsa_topk(logits, ld, P["row_len"], n, TOPK, P["sel"])
+            e[2].record(stream)
+            dsa.dsa_sparse_mla_decode_varlen(mla.q[j0:j0 + n], mla.kv, 64 * 576 * 2,
+                                             lay.num_pages, lay.block_table, ch["row_bt"], n,
+                                             P["sel"][:n], TOPK, mla.scale,
+                                             pst["out"][j0:j0 + n], pst["lse"][j0:j0 + n],
+                                             P["ws"], P["wsb"])
+            e[3].record(stream)
+            evs.append(e)
+        torch.cuda.synchronize()
+        for e in evs:
+            acc["indexer"] += e[0].elapsed_time(e[1])
+            acc["topk"] += e[1].elapsed_time(e[2])
+            acc["sparse_mla"] += e[2].elapsed_time(e[3])
+    return {k: v / reps for k, v in acc.items()}
 
 
 def time_prefill(pst, steps, warmup, stream):
@@ -497,43 +627,98 @@ def e2e_decode(st, steps, warmup, stream):
     return ms, h2d, d2h
 
 
-def cpu_baseline_sample(rows=16, threads=None, min_seconds=10.0):
-    """The oracle on a bounded sample of the headline workload: `rows` of the 64
-    query rows (indexer over their 131072 keys, full-sort top-2048 and the
-    sparse attention of those rows), repeated until at least `min_seconds` of
-    CPU time have run.  Returns (keys/s, cores, seconds, desc)."""
+# ---------------------------------------------------------- oracle timings --
+# The fp64 CPU oracle (test infrastructure) timed on this host's cores as the
+# reported baseline of each workload, on the very inputs the GPU legs ran
+# (copied to the host), with the samples the benchmark spec plans: the tiny decode,
+# the batched varlen path and the candidate path in full, all 64 rows of the
+# 128K step, and 64 of the 4096 prefill rows (extrapolated by their (row,
+# key) pairs).
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _bits(t):
     import numpy as np
-    import torch
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    return W.bf16_bits(t).cpu().numpy().view(np.uint16)
+
+
+def oracle_dense_path(case, next_n, mla, th, rows=None):
+    """Indexer + full-sort top-2048 (+ sparse MLA over the oracle's own
+    selection when `mla` is given) of `rows` (all by default) of a dense
+    workload.  Returns (seconds, (row, key) pairs, rows)."""
+    import numpy as np
     import oracle
     from deepseek_sparse_attention_02_gb300 import workloads as W
-    nreq = max(1, (rows + 1) // 2)
-    case = W.make_indexer_case([131072] * nreq, next_n=2, seed=0, device="cpu")
-    mla = W.make_mla_case(case.rows, case.layout.num_pages, seed=0, device="cpu")
-    sel_rows = np.arange(min(rows, case.rows), dtype=np.int32)
-    th = threads or oracle.hardware_threads()
-    cache = case.cache.numpy().reshape(-1)
-    q_bits = W.bf16_bits(mla.q).numpy().view(np.uint16)
-    kv_bits = W.bf16_bits(mla.kv).numpy().view(np.uint16)
-    L = oracle.row_lengths(case.layout.ctx_len.numpy(), 2)[sel_rows]
-    reps, dt = 0, 0.0
-    while reps == 0 or dt < min_seconds:
-        t0 = time.perf_counter()
-        ref, _ = oracle.indexer_logits(case.q.numpy(), case.q_scale.numpy(), case.w.numpy(),
-                                       cache, W.FP8_PAGE_BYTES, cache[W.FP8_KEY_BYTES:],
-                                       W.FP8_PAGE_BYTES, 64, case.layout.block_table.numpy(),
-                                       case.layout.ctx_len.numpy(), 2, rows=sel_rows, nthreads=th)
-        idx_sel = oracle.topk(ref, L, TOPK, nthreads=th)
+    sel = np.arange(case.rows, dtype=np.int32) if rows is None else np.asarray(rows, np.int32)
+    ctx = _np(case.layout.ctx_len)
+    L = oracle.row_lengths(ctx, next_n)[sel]
+    cache = _np(case.cache).reshape(-1)
+    bt = _np(case.layout.block_table)
+    q, qs, w = _np(case.q), _np(case.q_scale), _np(case.w)
+    if mla is not None:
+        q_bits, kv_bits = _bits(mla.q), _bits(mla.kv)
+    t0 = time.perf_counter()
+    ref, _ = oracle.indexer_logits(q, qs, w, cache, W.FP8_PAGE_BYTES, cache[W.FP8_KEY_BYTES:],
+                                   W.FP8_PAGE_BYTES, 64, bt, ctx, next_n, rows=sel, nthreads=th)
+    idx = oracle.topk(ref, L, TOPK, nthreads=th)
+    if mla is not None:
         idx_full = np.full((case.rows, TOPK), -1, np.int32)
-        idx_full[sel_rows] = idx_sel
-        oracle.sparse_mla(q_bits, kv_bits, 64 * 576, 64, case.layout.block_table.numpy(), 2,
-                          idx_full, mla.scale, rows=sel_rows, nthreads=th)
-        dt += time.perf_counter() - t0
-        reps += 1
-    keys = float(L.sum()) * reps
-    desc = (f"{len(sel_rows)} of the 64 query rows (131071/131072 keys each), run {reps} times: "
-            f"oracle indexer, full-sort top-2048 and sparse MLA of those rows; "
-            f"keys/s = their keys / time")
-    return keys / dt, th, dt, desc
+        idx_full[sel] = idx
+        oracle.sparse_mla(q_bits, kv_bits, 64 * 576, 64, bt, next_n, idx_full, mla.scale, rows=sel,
+                          nthreads=th)
+    return time.perf_counter() - t0, float(L.sum()), len(sel)
+
+
+def oracle_candidate_path(cst, th):
+    """The candidate path in full: one expansion, then the 4 consumer layers'
+    MXFP4 candidate logits and the top-2048 over them.  Returns (seconds,
+    candidate (row, column) pairs scored)."""
+    import oracle
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    cand = _np(cst["cand"])
+    ctx = _np(cst["layers"][0].layout.ctx_len)
+    layers = [(_np(c.q), _np(c.q_scale), _np(c.w), _np(c.cache).reshape(-1),
+               _np(c.layout.block_table)) for c in cst["layers"]]
+    t0 = time.perf_counter()
+    si, end = oracle.candidate_expand(cand, 64, ctx, 1)
+    for q, qs, w, cache, bt in layers:
+        lg, _ = oracle.candidate_logits(q, qs, w, cache, W.FP4_PAGE_BYTES, cache[W.FP4_KEY_BYTES:],
+                                        W.FP4_PAGE_BYTES, 64, bt, 1, si, 64, end, nthreads=th)
+        oracle.topk(lg, end, TOPK, col_blocks=si, bs=64, nthreads=th)
+    return time.perf_counter() - t0, float(end.sum()) * len(layers)
+
+
+def oracle_baselines(th, st, dense, cst, pst):
+    """Every workload's oracle time on this host (the plan above), on the
+    inputs of the GPU legs that ran."""
+    import numpy as np
+    out = {}
+    for d in dense:
+        name = "tiny_decode" if d["cfg"] == 0 else "batched_varlen"
+        dt, keys, n = oracle_dense_path(d["case"], d["next_n"], d["mla"], th)
+        out[name] = {"seconds": round(dt, 3), "keys_per_s": keys / dt,
+                     "sample": f"all {n} rows (full workload)"}
+    dt, keys, n = oracle_dense_path(st["case"], 2, st["mla"], th)
+    out["mtp_128k"] = {"seconds": round(dt, 3), "keys_per_s": keys / dt,
+                       "sample": f"all {n} rows (full workload)"}
+    if cst is not None:
+        dt, keys = oracle_candidate_path(cst, th)
+        out["candidate"] = {"seconds": round(dt, 3), "keys_per_s": keys / dt,
+                            "sample": "full workload (1 expansion + 4 layers)"}
+    if pst is not None:
+        nq, ctx = pst["nq"], pst["ctx"]
+        rng = np.random.default_rng(4)
+        rows = np.unique(np.concatenate([[0, nq - 1], rng.choice(nq, 62, replace=False)]))[:64]
+        dt, keys, n = oracle_dense_path(pst["case"], nq, pst["mla"], th, rows=rows)
+        total = sum(ctx - (nq - 1 - j) for j in range(nq))
+        out["prefill"] = {"seconds_sample": round(dt, 3), "keys_per_s": keys / dt,
+                          "seconds_full_extrapolated": round(dt * total / keys, 1),
+                          "sample": f"{n} of the {nq} query rows (first, last, seeded middle); "
+                                    "full time extrapolated by (row, key) pairs"}
+    return out
 
 
 def dist_setup():
@@ -588,11 +773,14 @@ def run_ours(args):
     ckernels16 = [] if cst is None else candidate_kernels(cst, bf16=True)
     lst = None if args.no_layers else build_layers(st)
     pst = None if args.no_prefill else build_prefill(device)
+    dense = [] if args.no_configs else [build_dense_config(device, cfg) for cfg in (0, 1)]
     torch.cuda.synchronize()
 
     barrier(pg, device)
     with ClockSampler(local) as clocks:
         total_ms, per = time_kernels(kernels, args.steps, args.warmup, stream)
+        dense_res = [time_kernels(dense_config_kernels(d), args.steps, args.warmup, stream)
+                     for d in dense]
         if ckernels:
             c_total_ms, c_per = time_kernels(ckernels, args.steps, args.warmup, stream)
             c16_total_ms, c16_per = time_kernels(ckernels16, args.steps, args.warmup, stream)
@@ -600,6 +788,7 @@ def run_ours(args):
             lay_ms, lay_launches = time_layers(st, lst, args.steps, args.warmup, stream)
         if pst is not None:
             pre_ms, pre_launches = time_prefill(pst, args.steps, args.warmup, stream)
+            pre_kms = prefill_kernel_ms(pst, "one_chunk", max(1, args.steps // 4), stream)
     barrier(pg, device)
     torch.cuda.synchronize()
     assert dsa.dsa_get_device_error() == 0, "device error word set during the benchmark"
@@ -609,6 +798,10 @@ def run_ours(args):
     keys_per_step = float(st["L"].sum().item())
     value = aggregate_value(world, keys_per_step, ms_step_max)
     hbm, bf16_tf, peak_src = peaks()
+    dense_out = {}
+    for d, (tms, dper) in zip(dense, dense_res):
+        name = "tiny_decode" if d["cfg"] == 0 else "batched_varlen"
+        dense_out[name] = dense_metrics(d, tms, dper, args.steps, hbm, bf16_tf)
     # dominant kernel: the indexer (HBM-bound): 128 B key + 4 B scale per cached
     # token read, 4 B logit per (row, key) written
     tokens = args.requests * 131072
@@ -642,7 +835,12 @@ def run_ours(args):
                 "breakdown_ms": {k: round(v, 4) for k, v in c_per.items()},
                 "candidate_keys_per_s": cand_keys / (c_ms * 1e-3),
                 "logits_hbm_gbs": c_bytes / (c_log * 1e-3) / 1e9,
+                # 64 B packed key + 4 B UE8M0 scales read + 4 B logit written per column
+                "logits_hbm_frac": round(c_bytes / (c_log * 1e-3) / 1e9 / hbm, 4),
                 "topk_rows_per_s": cst["R"] / (ctk * 1e-3),
+                "topk_frac": round(kernel_roofline(float(cst["end"].sum().item()) * 4 +
+                                                   cst["R"] * TOPK * 4, 0.0, ctk, hbm,
+                                                   bf16_tf)["frac"], 4),
                 "bf16_logits": {
                     "ms_per_step": c16_total_ms / args.steps,
                     "breakdown_ms": {k: round(v, 4) for k, v in c16_per.items()},
@@ -671,8 +869,51 @@ def run_ours(args):
                                "keys_per_s": pairs / (pre_ms["chunked"] * 1e-3)},
                    "one_chunk": {"logits_bytes": nrows * ctxn * 4,
                                  "ms": round(pre_ms["one_chunk"], 4),
-                                 "keys_per_s": pairs / (pre_ms["one_chunk"] * 1e-3)}}
+                                 "keys_per_s": pairs / (pre_ms["one_chunk"] * 1e-3),
+                                 "breakdown_ms": {k: round(v, 4) for k, v in pre_kms.items()}}}
+        # tensor-pipe fractions of the one-chunk launches: the indexer's FP8
+        # contraction (2 * 64 * 128 flops per (row, key)) against twice the
+        # measured bf16 burst (the nominal FP8 : bf16 dense ratio), the
+        # attention's bf16 contractions (2 * 128 * k * (576 + 512) per row)
+        # against the bf16 burst
+        idx_flops = pairs * 2 * 64 * 128
+        mla_flops_p = nrows * 2 * 128 * TOPK * (576 + 512)
+        prefill["one_chunk"]["indexer_tensor_frac"] = round(
+            idx_flops / (pre_kms["indexer"] * 1e-3) / 1e12 / (2 * bf16_tf), 4)
+        prefill["one_chunk"]["sparse_mla_tensor_frac"] = round(
+            mla_flops_p / (pre_kms["sparse_mla"] * 1e-3) / 1e12 / bf16_tf, 4)
+        prefill["one_chunk"]["attended_tok_per_s"] = nrows * TOPK / (pre_kms["sparse_mla"] * 1e-3)
 
+    topk_rf = kernel_roofline(topk_bytes, 0.0, per["topk"], hbm, bf16_tf)
+    mla_rf = kernel_roofline(mla_bytes, mla_flops, per["sparse_mla"], hbm, bf16_tf)
+    kernels_rf = {"topk": {"frac": round(topk_rf["frac"], 4), "bound": "hbm",
+                           "measured_us": round(topk_rf["measured_us"], 2),
+                           "roofline_us": round(topk_rf["roofline_us"], 2)},
+                  "sparse_mla": {"frac": round(mla_rf["frac"], 4), "bound": mla_rf["bound"],
+                                 "measured_us": round(mla_rf["measured_us"], 2),
+                                 "roofline_us": round(mla_rf["roofline_us"], 2)}}
+    if cand is not None:
+        kernels_rf["candidate_logits"] = {"frac": cand["logits_hbm_frac"], "bound": "hbm"}
+        kernels_rf["candidate_topk"] = {"frac": cand["topk_frac"], "bound": "hbm"}
+    if prefill is not None:
+        kernels_rf["prefill_indexer"] = {"frac": prefill["one_chunk"]["indexer_tensor_frac"],
+                                         "bound": "tensor (fp8 = 2 x bf16 burst)"}
+        kernels_rf["prefill_sparse_mla"] = {
+            "frac": prefill["one_chunk"]["sparse_mla_tensor_frac"], "bound": "tensor (bf16 burst)"}
+    for name, d in dense_out.items():
+        kernels_rf[f"{name}_indexer"] = {"frac": d["indexer_hbm_frac"], "bound": "hbm"}
+        kernels_rf[f"{name}_topk"] = {"frac": d["topk_frac"], "bound": "hbm"}
+        if "sparse_mla_frac" in d:
+            kernels_rf[f"{name}_sparse_mla"] = {"frac": d["sparse_mla_frac"], "bound": "max"}
+    fr = {"indexer_hbm_frac": achieved / hbm, "topk_frac": topk_rf["frac"],
+          "sparse_mla_frac": mla_rf["frac"]}
+    targets = {f"{k} >= {v:.2f}": {"value": round(fr[k], 4), "pass": bool(fr[k] >= v)}
+               for k, v in TARGETS.items()}
+    n_dense = sum(2 * args.steps * len(dense_config_kernels(d)) for d in dense)
+    n_pre = 0
+    if pst is not None:
+        P1 = pst["plans"]["one_chunk"]
+        n_pre = max(1, args.steps // 4) * len(P1["chunks"]) * (4 + (1 if P1["wsb"] > 0 else 0))
     line = {
         "metric": METRIC,
         "value": value,
@@ -693,29 +934,23 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({tokens * 132 / 1e6:.1f} MB key cache, "
                          f"{tokens * 1152 / 1e9:.1f} GB latent cache); no flush"},
-        "breakdown_ms": {k: round(v, 4) for k, v in per.items()},
+        "candidate_path": cand,
+        "layer_schedules": layers,
+        "prefill_chunks": prefill,
         "indexer": {"keys_per_s": keys_per_step / t_idx, "hbm_gbs": achieved,
                     "unique_keys_per_s": tokens / t_idx},
         "topk": {"rows_per_s": R / (per["topk"] * 1e-3),
                  "logit_gbs": keys_per_step * 4 / (per["topk"] * 1e-3) / 1e9,
-                 "roofline": kernel_roofline(topk_bytes, 0.0, per["topk"], hbm, bf16_tf)},
+                 "roofline": topk_rf},
         "sparse_mla": {"attended_tok_per_s": R * TOPK / (per["sparse_mla"] * 1e-3),
                        "gather_gbs": R * TOPK * 1152 / (per["sparse_mla"] * 1e-3) / 1e9,
                        "tflops": mla_flops / (per["sparse_mla"] * 1e-3) / 1e12,
-                       "roofline": kernel_roofline(mla_bytes, mla_flops, per["sparse_mla"], hbm,
-                                                   bf16_tf)},
-        "candidate_path": cand,
-        "layer_schedules": layers,
-        "prefill_chunks": prefill,
-        "roofline": {"kernel": "dsa_indexer_logits", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                     "peak_source": peak_src,
-                     "alg_bytes_per_launch": alg_bytes},
+                       "roofline": mla_rf},
         # time_kernels times the plain passes and the event-instrumented ones
         "gpu_launches": 2 * args.steps * (len(kernels) + (1 if st["wsb"] > 0 else 0)) +
                         2 * (args.steps * (len(ckernels) + 1) if ckernels else 0) * 2 +
                         (lay_launches if lst is not None else 0) +
-                        (pre_launches if pst is not None else 0),
+                        (pre_launches if pst is not None else 0) + n_dense + n_pre,
         "e2e": {"value": world * keys_per_step / (e2e_ms * 1e-3), "unit": "keys/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "pinned host; step i+1's inputs and step i-1's outputs copied while "
@@ -723,34 +958,57 @@ def run_ours(args):
                 "serial": {"value": world * keys_per_step / (e2e_serial_ms * 1e-3),
                            "ms_per_step": e2e_serial_ms}},
         "clocks": clocks.summary(),
+        # the per-workload figures last (the end of the line is what a reader
+        # of a truncated log sees)
+        "configs": dense_out,
+        "breakdown_ms": {k: round(v, 4) for k, v in per.items()},
+        "roofline": {"kernel": "dsa_indexer_logits", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "peak_source": peak_src, "alg_bytes_per_launch": alg_bytes,
+                     "kernels": kernels_rf, "targets": targets},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, dt, desc = cpu_baseline_sample(rows=args.cpu_rows)
-        line["cpu_baseline"] = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+        th = _oracle_threads()
+        ob = oracle_baselines(th, st, dense, cst, pst)
+        line["cpu_baseline"] = {"value": ob["mtp_128k"]["keys_per_s"], "unit": "keys/s",
+                                "cores": th, "kind": "oracle",
+                                "sample": "the 128K MTP step's 64 rows in full (oracle indexer, "
+                                          "full-sort top-2048, sparse MLA); keys/s = (row, key) "
+                                          "pairs / time",
+                                "seconds": ob["mtp_128k"]["seconds"], "workloads": ob}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
 
 
+def _oracle_threads():
+    import oracle
+    return oracle.hardware_threads()
+
+
 def run_reference(args):
+    """The oracle (the reference arm of this build) on the headline workload:
+    each step is the 128K MTP step's 64 rows in full on the host cores."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
     oracle.build()
+    th = _oracle_threads()
     vals, dts = [], []
-    desc, cores = "", 1
-    # one pass of the sample per step, so that --steps K --warmup W ends in minutes
+    from deepseek_sparse_attention_02_gb300 import workloads as W
+    case = W.make_indexer_case([131072] * 32, next_n=2, seed=0, device="cpu")
+    mla = W.make_mla_case(case.rows, case.layout.num_pages, seed=0, device="cpu")
     for _ in range(args.warmup):
-        cpu_baseline_sample(rows=args.cpu_rows, min_seconds=0.0)
+        oracle_dense_path(case, 2, mla, th)
     for _ in range(args.steps):
-        v, cores, dt, desc = cpu_baseline_sample(rows=args.cpu_rows, min_seconds=0.0)
-        vals.append(v)
+        dt, keys, n = oracle_dense_path(case, 2, mla, th)
+        vals.append(keys / dt)
         dts.append(dt)
     value = statistics.mean(vals)
+    tokens = 32 * 131072
     line = {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
@@ -758,9 +1016,12 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": WORKLOAD, "global_batch": 64, "seq_len": 131072,
-                   "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": "keys/s", "cores": cores, "kind": "oracle",
-                         "sample": desc},
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({tokens * 132 / 1e6:.1f} MB key cache, "
+                         f"{tokens * 1152 / 1e9:.1f} GB latent cache); no flush"},
+        "cpu_baseline": {"value": value, "unit": "keys/s", "cores": th, "kind": "oracle",
+                         "sample": "the 128K MTP step's 64 rows in full per step (oracle indexer, "
+                                   "full-sort top-2048, sparse MLA)"},
         "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -772,7 +1033,6 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--requests", type=int, default=32,
                     help="decode requests (32 = the 128K workload; fewer for profiling)")
@@ -782,6 +1042,8 @@ def build_parser() -> argparse.ArgumentParser:
                     help="skip the multi-layer IndexCache / MLI schedule measurement")
     ap.add_argument("--no-candidate", action="store_true",
                     help="skip the candidate-path leg (profiling)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the tiny-decode and batched-varlen legs (profiling)")
     return ap
 
 

@@ -321,10 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       if (warp == 0) tma_prefetch_desc(&tm_q);
     }
-    // The key cache is read once per step: its lines go first out of L2, which
-    // leaves the logits this kernel writes in L2 for the top-k that reads them
-    // next.
-    const uint64_t evict_first = l2_policy_evict_first();
+    // Decode (at most 2 rows per group) reads the key cache once per step: its
+    // lines go first out of L2, which leaves the logits this kernel writes in
+    // L2 for the top-k that reads them next.  A prefill chunk (4 rows per
+    // group) reads the same keys once per row group: they stay in L2 instead.
+    const uint64_t key_policy = G <= 2 ? l2_policy_evict_first() : l2_policy_evict_last();
     // Page ids of a chunk (at most 2 * kChunkTiles) are loaded by the lanes of
     // this warp one chunk ahead, so no block-table load sits on the TMA issue path.
     auto chunk_pages = [&](const Cursor& c) -> int {
@@ -386,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               page = 0;
             }
             tma_load_3d_hint(s.keys[st] + h * kPageKeyBytes, &tm_k, &s.full[st], 0, 0, page,
-                             evict_first);
+                             key_policy);
             bulk_load_hint(&s.scales[st][h * 64],
                            p.k_scale + static_cast<int64_t>(page) * p.s_page_stride, 256,
-                           &s.full[st], evict_first);
+                           &s.full[st], key_policy);
           }
         }
         __syncwarp();

@@ -127,6 +127,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
+// L2 policy that marks the lines it is attached to as last to evict: for data
+// every CTA reads again and again (a prefill chunk's key cache, read by each of
+// its row groups), so that a long stream of other lines does not push it out.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // 3-D tiled TMA load (one box at coordinates c0, c1, c2) with an L2 cache
 // policy attached to the read.
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
