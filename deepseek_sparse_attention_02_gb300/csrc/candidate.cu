@@ -12,12 +12,15 @@
 // candidate_logits: the indexer pipeline of indexer.cu over candidate
 // columns.  A tile is 128 sparse columns = two candidate blocks = two
 // 64-token pages, fetched by cp.async.bulk (4096 packed bytes + 256 scale
-// bytes each).  The owning epilogue warpgroup expands e2m1 -> e4m3 (exact: every
-// e2m1 value is an e4m3 value) into a 128B-swizzled [128 x 128] tile with two
-// byte-permute lookups per 4 elements.  The MMA warp then issues one
-// kind::f8f6f4 MMA per 32-element scale group (K = 32) into four TMEM
-// accumulators, so the epilogue applies the UE8M0 scales exactly:
-//   logit = sum_h w'_h * ReLU(sum_g 2^(e_g - 127) * D_g[h]).
+// bytes each).  Converter warps expand e2m1 -> e4m3 (exact: every e2m1 value is
+// an e4m3 value) into a 128B-swizzled [128 x 128] tile with two byte-permute
+// lookups per 4 elements, and put each token's four UE8M0 scale bytes (one per
+// 32-element group) into a tensor-memory column.  The MMA warp then issues
+// four block-scaled kind::mxf8f6f4 MMAs (K = 32 each, the group g one taking
+// byte g of the token's scale word, the q side scaled by 2^0) into one
+// accumulator, so the tensor core applies the scales:
+//   logit = sum_h w'_h * ReLU(sum_g 2^(e_g - 127) * (k'_g . q'_g)[h]),
+// and the epilogue is the dense indexer's (one accumulator, ReLU, weights).
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -28,13 +31,26 @@
 namespace dsa {
 namespace {
 
-// warp 0 producer, warp 1 MMA issuer, warps 2-5 converters, warps 6-13 two
-// epilogue warpgroups
+// warp 0 producer, warp 1 MMA issuer, warps 2-9 two converter groups (group
+// g converts the tiles == g mod 2, so two tiles are converted at once: one
+// group alone, converting a tile after the other, set the kernel's pace),
+// warps 10-13 the epilogue warpgroup (one accumulator per tile: light work)
 constexpr int kConvWarp = 2;
-constexpr int kFirstEpiWarp = 6;
-constexpr int kThreads = 32 * (kFirstEpiWarp + 8);
+constexpr int kFirstEpiWarp = 10;
+constexpr int kThreads = 32 * (kFirstEpiWarp + 4);
 constexpr int kStages = 8;  // raw (packed + scale) stages
-constexpr int kA = 4;       // converted e4m3 tiles; even, so a slot has one epilogue warpgroup
+constexpr int kA = 4;       // converted e4m3 tiles (and their scale columns)
+static_assert(kA % 2 == 0 && kStages % 2 == 0,
+              "a stage and a converted slot always belong to the same converter group");
+constexpr int kAcc = 4;     // [128 x 64] accumulators; even: accumulator a is drained by warpgroup a % 2
+// Tensor-memory columns: the accumulators, then a 4-column scale block per
+// converted tile slot (row m of the tile: column m / 32, lane m % 32 in every
+// lane quadrant, byte g = the scale of its group g), then the q side's scale
+// block (every byte 2^0); each block 16-column aligned.
+constexpr uint32_t kSfaCol = 64 * kAcc;
+constexpr uint32_t kSfStride = 16;
+constexpr uint32_t kSfbCol = kSfaCol + kSfStride * kA;
+constexpr uint32_t kOneScales = 0x7F7F7F7Fu;  // four UE8M0 bytes of 2^0
 constexpr int kTileCols = 128;
 constexpr int kChunkTiles = 4;
 constexpr uint32_t kPackedPage = 64 * 64;  // 4096
@@ -163,6 +179,7 @@ struct CParams {
   float* logits;          // f32 output, or
   uint16_t* logits_bf16;  // bf16 output (round to nearest even) when not null
   int64_t ld;
+  int packed;             // each page's scales follow its keys (one copy per page)
   uint32_t* err;
 };
 
@@ -217,13 +234,15 @@ struct RowCursor {
 struct CSmem {
   uint8_t a[kA][128 * 128];          // converted e4m3 key tiles, K-major SW128
   uint8_t q[2][64 * 128];            // q of the row, K-major SW128
-  uint8_t raw[kStages][2 * kPackedPage];
+  // a stage's two pages: keys at raw + h * kPackedPage and scales at sf + h *
+  // kSfPage, or (pages with the scales right after the keys) the whole page at
+  // raw + h * (kPackedPage + kSfPage)
+  uint8_t raw[kStages][2 * (kPackedPage + kSfPage)];
   uint8_t sf[kStages][2 * kSfPage];
   float wq[2][64];
   uint64_t full[kStages], empty[kStages];
   uint64_t qfull[2], qempty[2];
-  uint32_t ascale[kA][128];          // UE8M0 scale words of each converted tile's rows
-  uint64_t afull[kA], aempty[kA], tfull[2], tempty[2];
+  uint64_t afull[kA], aempty[kA], tfull[kAcc], tempty[kAcc];
   uint32_t tmem_base;
   int abort;
 };
@@ -239,14 +258,10 @@ __device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t x) {
   return mag | (neg & 0x80808080u);
 }
 
-__device__ __forceinline__ float ue8m0_to_float(uint32_t e) {
-  return e == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     candidate_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const CParams p) {
-  constexpr uint32_t kTmemCols = 512;  // two buffers of four [128 x 64] accumulators
-  constexpr uint32_t kIdesc = make_idesc(0, 0, 128, 64, false, false);
+  constexpr uint32_t kTmemCols = 512;  // accumulators + scale columns, rounded up to a power of 2
+  static_assert(kSfbCol + 4 <= kTmemCols, "tensor-memory columns");
   extern __shared__ uint8_t smem_raw[];
   CSmem& s = *reinterpret_cast<CSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
@@ -258,21 +273,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 4);  // the 4 converter warps
+      mbar_init(&s.empty[i], 4);  // the 4 warps of the converter group of the stage's tile
     }
     for (int i = 0; i < kA; ++i) {
-      mbar_init(&s.afull[i], 4);      // the 4 converter warps
-      mbar_init(&s.aempty[i], 1 + 4); // MMA commit + the 4 epilogue warps that read the scales
+      mbar_init(&s.afull[i], 4);   // the 4 converter warps of the tile's group
+      mbar_init(&s.aempty[i], 1);  // the MMA commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.qfull[i], 32);
-      mbar_init(&s.qempty[i], 1 + 8);
+      mbar_init(&s.qempty[i], 1 + 4);  // the MMA commit + the 4 epilogue warps
+    }
+    for (int i = 0; i < kAcc; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);
+      mbar_init(&s.tempty[i], 4);  // the 4 epilogue warps
     }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // the q side's scale block: every byte 2^0, in all 128 lanes (the four
+  // epilogue warps cover the four lane quadrants)
+  if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4)
+    tmem_st4_sync(s.tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfbCol,
+                  kOneScales, kOneScales, kOneScales, kOneScales);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -339,23 +364,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pid[2];
         pid[0] = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb));
         pid[1] = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb) + 1);
-        if (lane == 0) {
-          const bool two = (2 * t + 1) * 64 < endr;
+        const bool two = (2 * t + 1) * 64 < endr;
+        if (lane == 0)
           mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kPackedPage + kSfPage));
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (h == 1 && !two) break;
+        __syncwarp();
+        // the tile's copies go out from different lanes: one thread's bulk
+        // copies are taken one after another (~500 cycles each on GB300)
+        if (lane < 4) {
+          const int h = lane >> 1;  // which page of the tile
+          const bool sf = (lane & 1) != 0;
+          if (h == 0 || two) {
             int page = pid[h];
             if (page < 0 || page >= p.num_pages) {
-              raise_error(p.err, kErrBadPage);
+              if (!sf) raise_error(p.err, kErrBadPage);
               page = 0;
             }
-            bulk_load_hint(s.raw[st] + h * kPackedPage,
-                           p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride, kPackedPage,
-                           &s.full[st], evict_first);
-            bulk_load_hint(s.sf[st] + h * kSfPage,
-                           p.k_sf + static_cast<int64_t>(page) * p.sf_page_stride, kSfPage,
-                           &s.full[st], evict_first);
+            if (p.packed) {
+              // keys and scales contiguous: one copy of the page's 4352 bytes
+              if (!sf)
+                bulk_load_hint(s.raw[st] + h * (kPackedPage + kSfPage),
+                               p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride,
+                               kPackedPage + kSfPage, &s.full[st], evict_first);
+            } else if (!sf) {
+              bulk_load_hint(s.raw[st] + h * kPackedPage,
+                             p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride, kPackedPage,
+                             &s.full[st], evict_first);
+            } else {
+              bulk_load_hint(s.sf[st] + h * kSfPage,
+                             p.k_sf + static_cast<int64_t>(page) * p.sf_page_stride, kSfPage,
+                             &s.full[st], evict_first);
+            }
           }
         }
         __syncwarp();
@@ -384,17 +422,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b0 = smem_u32(s.q[slot]);
         for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
           const int ac = lt % kA;
-          const int buf = lt & 1;
-          const int ub = lt >> 1;
+          const int buf = lt % kAcc;
+          const int ub = lt / kAcc;
           if (!mbar_wait(&s.afull[ac], (lt / kA) & 1, p.err, abort)) { bad = true; break; }
           if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(s.a[ac]);
-          const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * 256);
+          const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * 64);
+          const uint32_t sfa = s.tmem_base + kSfaCol + kSfStride * static_cast<uint32_t>(ac);
+          const uint32_t sfb = s.tmem_base + kSfbCol;
 #pragma unroll
           for (int g = 0; g < 4; ++g)
-            mma_f8f6f4(d + 64 * g, sw128_desc(a0 + 32 * g, 16, 1024),
-                       sw128_desc(b0 + 32 * g, 16, 1024), kIdesc, 0);
+            mma_mxf8f6f4_bs(d, sw128_desc(a0 + 32 * g, 16, 1024), sw128_desc(b0 + 32 * g, 16, 1024),
+                            make_idesc_bs(0, 0, 128, 64, static_cast<uint32_t>(g), 0u), sfa, sfb,
+                            g > 0 ? 1u : 0u);
           mma_commit(&s.aempty[ac]);
           mma_commit(&s.tfull[buf]);
         }
@@ -409,9 +450,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A warp expands 8 token rows per step: lane l takes 16 packed bytes
     // (piece l % 4 of row l / 4; a warp's loads are 512 contiguous bytes) and
     // writes the 32 e4m3 bytes they expand to (two 16-byte chunks of the
-    // 128B-swizzled row; balanced over the banks).  Each warp also passes on
-    // the UE8M0 scale words of its 32 rows with the tile.
-    const int cw = warp - kConvWarp;  // rows [32 cw, 32 cw + 32) of every tile
+    // 128B-swizzled row; balanced over the banks).  Each warp also writes the
+    // slot's scale block into the TMEM lane quadrant it may access (warp % 4):
+    // lane l, columns j = 0..3 take the scale words of rows 32 j + l, so every
+    // quadrant holds the whole block.
+    const int cw = warp & 3;  // rows [32 cw, 32 cw + 32) of every tile
+    const int grp = (warp - kConvWarp) >> 2;  // converts the tiles == grp (mod 2)
+    const int key_stride = p.packed ? static_cast<int>(kPackedPage + kSfPage) : static_cast<int>(kPackedPage);
+    const int sf_stride = p.packed ? static_cast<int>(kPackedPage + kSfPage) : static_cast<int>(kSfPage);
     const int piece = lane & 3;
     RowCursor cur;
     cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
@@ -419,16 +465,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (cur.valid() && !*abort) {
       bool bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        if ((lt & 1) != grp) continue;
         const int st = lt % kStages;
         const int ac = lt % kA;
         if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
         if (lt >= kA && !mbar_wait_warp(&s.aempty[ac], ((lt / kA) - 1) & 1, p.err, abort)) { bad = true; break; }
         uint8_t* dst = s.a[ac];
+        const uint8_t* sf_base = p.packed ? s.raw[st] + kPackedPage : s.sf[st];
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int tr = 32 * cw + 8 * it + (lane >> 2);
           const uint4 v = *reinterpret_cast<const uint4*>(
-              s.raw[st] + (tr >> 6) * kPackedPage + (tr & 63) * 64 + 16 * piece);
+              s.raw[st] + (tr >> 6) * key_stride + (tr & 63) * 64 + 16 * piece);
           const uint32_t in[4] = {v.x, v.y, v.z, v.w};
           uint32_t o[8];
 #pragma unroll
@@ -442,11 +490,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(o[4], o[5], o[6], o[7]);
         }
         {
-          const int tr = 32 * cw + lane;
-          s.ascale[ac][tr] =
-              *reinterpret_cast<const uint32_t*>(s.sf[st] + (tr >> 6) * kSfPage + (tr & 63) * 4);
+          uint32_t sfw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int tr = 32 * j + lane;
+            sfw[j] = *reinterpret_cast<const uint32_t*>(sf_base + (tr >> 6) * sf_stride +
+                                                        (tr & 63) * 4);
+          }
+          tmem_st4_sync(s.tmem_base + (static_cast<uint32_t>(32 * cw) << 16) + kSfaCol +
+                            kSfStride * static_cast<uint32_t>(ac),
+                        sfw[0], sfw[1], sfw[2], sfw[3]);
         }
         fence_proxy_async_smem();  // generic-proxy writes of the tile -> tensor core
+        tc_fence_before();         // the scale column -> the MMA issuer
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&s.afull[ac]);
@@ -458,7 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue --
-    const int wg = (warp - kFirstEpiWarp) >> 2;  // drains the tiles (and accumulator) == wg (mod 2)
     const int quad = warp & 3;
     const int tr = quad * 32 + lane;  // token row of the tile == TMEM lane
     RowCursor cur;
@@ -470,54 +525,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int endr = min(p.end[r], p.nb * 64);
       bool waited_q = false, bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
-        if ((lt & 1) != wg) continue;
-        const int ac = lt % kA;
         if (!waited_q) {
           if (!mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
           waited_q = true;
         }
-        if (!mbar_wait_warp(&s.tfull[wg], (lt >> 1) & 1, p.err, abort)) { bad = true; break; }
+        const int buf = lt % kAcc;
+        if (!mbar_wait_warp(&s.tfull[buf], (lt / kAcc) & 1, p.err, abort)) { bad = true; break; }
         tc_fence_after();
-        const uint32_t sfw = s.ascale[ac][tr];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.aempty[ac]);
-        float sc[4];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) sc[g] = ue8m0_to_float((sfw >> (8 * g)) & 0xffu);
         const uint32_t taddr = s.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(wg * 256);
-        float acc[2] = {0.f, 0.f};
-#pragma unroll
-        for (int hc = 0; hc < 4; ++hc) {
-          float d0[16], d1[16], d2[16], d3[16];
-          tmem_ld16_sync(taddr + 0 * 64 + 16 * hc, d0);
-          tmem_ld16_sync(taddr + 1 * 64 + 16 * hc, d1);
-          tmem_ld16_sync(taddr + 2 * 64 + 16 * hc, d2);
-          tmem_ld16_sync(taddr + 3 * 64 + 16 * hc, d3);
-          const float* wh = s.wq[slot] + 16 * hc;
-#pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const float x = fmaf(sc[3], d3[h], fmaf(sc[2], d2[h], fmaf(sc[1], d1[h], sc[0] * d0[h])));
-            acc[h & 1] = fmaf(wh[h], fmaxf(x, 0.f), acc[h & 1]);
-          }
-        }
+                               static_cast<uint32_t>(buf * 64);
+        float v[64];
+        tmem_ld64_sync(taddr, v);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.tempty[wg]);
+        if (lane == 0) mbar_arrive(&s.tempty[buf]);
+        // four partial sums: a single 64-long FMA chain is latency bound
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float* wh = s.wq[slot];
+#pragma unroll
+        for (int h = 0; h < 64; ++h) a4[h & 3] = fmaf(wh[h], fmaxf(v[h], 0.f), a4[h & 3]);
+        const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
         const int col = t * kTileCols + tr;
         if (col < endr) {
           const int64_t o = static_cast<int64_t>(r) * p.ld + col;
           if (p.logits_bf16)
-            p.logits_bf16[o] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[0] + acc[1]));
+            p.logits_bf16[o] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
           else
-            p.logits[o] = acc[0] + acc[1];
+            p.logits[o] = acc;
         }
       }
       if (bad) break;
-      // A warp may walk through a group without processing any of its tiles (they
-      // went to the other warpgroup).  It still waits for that group's Q before it
-      // arrives on the slot's qempty, so its arrival cannot land in the phase of
-      // the group that used the slot two groups earlier.
+      // A group without tiles here still has its Q waited for before the
+      // slot's qempty arrival, so the arrival cannot land in the phase of the
+      // group that used the slot two groups earlier.
       if (!waited_q && !mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
       const int gslot = slot;
       const bool left = cur.next();
@@ -580,6 +620,7 @@ cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& d
   p.logits = a.logits;
   p.logits_bf16 = a.logits_bf16;
   p.ld = a.ld;
+  p.packed = (a.k_sf == a.k_fp4 + kPackedPage && a.sf_page_stride == a.k_page_stride) ? 1 : 0;
   p.err = dev.err_word;
   // at least 120 KB so that one CTA (holding all 512 TMEM columns) runs per SM
   const size_t smem = sizeof(CSmem) + 1024 > 120 * 1024 ? sizeof(CSmem) + 1024 : 120 * 1024;

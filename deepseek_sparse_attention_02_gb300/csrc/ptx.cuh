@@ -242,6 +242,47 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// Block-scaled D[tmem] (+)= (A * 2^(sfa-127)) * (B * 2^(sfb-127))^T for
+// kind::mxf8f6f4 with one UE8M0 scale per 32 elements of K (scale_vec::1X):
+// the K = 32 of one instruction take one scale per row of A and of B, read
+// from tensor memory: row m of a 128-row operand at lane m % 32 (of each
+// lane quadrant) and column m / 32 of its 4-column scale block, the byte of
+// the 32-bit cell that the instruction descriptor's scale-data id selects
+// (so one block holds the scales of 4 successive K groups).  A scale block's
+// first column is kept 16-column aligned.
+__device__ __forceinline__ void mma_mxf8f6f4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem,
+                                                uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of a block-scaled kind::mxf8f6f4 MMA (both operands
+// K-major, f32 accumulate): [4,6) B scale-data id, [7,10) A format, [10,13) B
+// format, [17,23) N>>3, [23] scale type (1 = UE8M0), [24,29) M>>4, [29,31) A
+// scale-data id.  Formats: e4m3 = 0.
+__host__ __device__ constexpr uint32_t make_idesc_bs(uint32_t a_fmt, uint32_t b_fmt, int m, int n,
+                                                     uint32_t a_sf_id, uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((static_cast<uint32_t>(n) >> 3) << 17) |
+         (1u << 23) | ((static_cast<uint32_t>(m) >> 4) << 24) | (a_sf_id << 29);
+}
+
+// Stores 4 consecutive 32-bit TMEM columns of this thread's lane (32 lanes per
+// warp) and waits for the stores to complete.
+__device__ __forceinline__ void tmem_st4_sync(uint32_t taddr, uint32_t v0, uint32_t v1,
+                                              uint32_t v2, uint32_t v3) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+      : "memory");
+}
+
 // Arrive once on an mbarrier when every tcgen05 op issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {

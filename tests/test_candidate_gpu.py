@@ -171,3 +171,31 @@ def test_candidate_bf16_logits_and_topk():
     exact = oracle.topk(got, E, k, col_blocks=np_(si), bs=64)
     for i in range(R):
         assert sorted(np_(sel)[i].tolist()) == sorted(exact[i].tolist()), f"row {i}"
+
+
+def test_candidate_logits_split_key_and_scale_buffers():
+    """Keys and UE8M0 scales in two separate buffers (each with its own page
+    stride) give the same logits, bit for bit, as the canonical page (scales
+    right after the keys, fetched as one copy per page)."""
+    from deepseek_sparse_attention_02_gb300 import dsa
+    ctx, next_n, nb = [64 * 40 + 9, 5000], 1, 24
+    case = W.make_indexer_case(ctx, next_n=next_n, seed=6, device="cuda", fmt="mxfp4")
+    cand = W.make_candidates(ctx, next_n, 64, nb, seed=6, device="cuda")
+    si, end, sched, nbytes = expand(cand, case.layout.ctx_len, next_n)
+    ld = nb * 64
+    ref = cand_logits(case, si, end, sched, nbytes, ld)
+    c = case.cache.view(-1, W.FP4_PAGE_BYTES)
+    keys = c[:, :W.FP4_KEY_BYTES].contiguous()
+    scales = torch.zeros((c.shape[0], 512), dtype=torch.uint8, device="cuda")  # stride 512
+    scales[:, :256] = c[:, W.FP4_KEY_BYTES:]
+    got = torch.full((case.rows, ld), float("nan"), device="cuda")
+    dsa.dsa_candidate_logits(case.q, case.q_scale, case.w, keys, W.FP4_KEY_BYTES, scales, 512,
+                             case.layout.num_pages, case.layout.block_table,
+                             len(case.layout.ctx_len), next_n, si, nb, 64, end, sched, nbytes,
+                             got, ld)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+    E = np_(end)
+    g, r = np_(got), np_(ref)
+    for i in range(case.rows):
+        assert np.array_equal(g[i, :E[i]].view(np.uint32), r[i, :E[i]].view(np.uint32)), i
