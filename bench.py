@@ -248,11 +248,11 @@ def dense_metrics(st, total_ms, per, steps, hbm, bf16_tf):
     return out
 
 
-def build_candidate(device, seed=3):
+def build_candidate(device, seed=3, requests=64):
     import torch
     from deepseek_sparse_attention_02_gb300 import dsa
     from deepseek_sparse_attention_02_gb300 import workloads as W
-    ctx = [196608] * 64
+    ctx = [196608] * requests
     layers = [W.make_indexer_case(ctx, next_n=1, seed=seed + i, device=device, fmt="mxfp4")
               for i in range(4)]
     cand = W.make_candidates(ctx, 1, 64, 512, seed=seed, device=device)
@@ -768,7 +768,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     st = build_decode(device, requests=args.requests)
     kernels = decode_kernels(st)
-    cst = None if args.no_candidate else build_candidate(device)
+    cst = None if args.no_candidate else build_candidate(device, requests=args.candidate_requests)
     ckernels = [] if cst is None else candidate_kernels(cst)
     ckernels16 = [] if cst is None else candidate_kernels(cst, bf16=True)
     lst = None if args.no_layers else build_layers(st)
@@ -829,7 +829,7 @@ def run_ours(args):
         c_log = statistics.mean(c_per[f"cand_logits_{i}"] for i in range(4))
         c_bytes = float(cst["end"].sum().item()) * 68 + float(cst["end"].sum().item()) * 4
         ctk = statistics.mean(c_per[f"cand_topk_{i}"] for i in range(4))
-        cand = {"workload": "64 requests x 196608 ctx, 512 candidate blocks of 64, "
+        cand = {"workload": f"{cst['R']} requests x 196608 ctx, 512 candidate blocks of 64, "
                             "MXFP4 keys, 1 expansion + 4 consumer layers (logits + top-2048)",
                 "ms_per_step": c_ms,
                 "breakdown_ms": {k: round(v, 4) for k, v in c_per.items()},
@@ -1044,6 +1044,8 @@ def build_parser() -> argparse.ArgumentParser:
                     help="skip the candidate-path leg (profiling)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the tiny-decode and batched-varlen legs (profiling)")
+    ap.add_argument("--candidate-requests", type=int, default=64,
+                    help="candidate-path requests (64 = the candidate workload; fewer for profiling)")
     return ap
 
 

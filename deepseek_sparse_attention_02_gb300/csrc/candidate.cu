@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int blk2 = load_blk(ahead2);
     int pages1 = load_page(ahead1, blk1);
     int lt = 0, endr = 0;
+    int q_issued[2] = {0, 0};  // Q loads issued into each slot
     bool new_group = true;
     while (cur.valid() && !*abort) {
       const int r = cur.row;
@@ -353,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           mbar_arrive(&s.qfull[slot]);
         }
+        ++q_issued[slot];
       }
       if (new_group) endr = min(p.end[r], p.nb * 64);
       const int tb = cur.tile_begin();
@@ -407,6 +409,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       blk2 = load_blk(ahead2);
       pages1 = load_page(ahead1, blk1);
     }
+    // every copy issued has landed before the CTA can exit (at once unless a
+    // wait ran out and the consumers stopped early); tile i used stage i mod
+    // kStages, so the last lt tiles' phases are the ones to wait for
+    if (lane == 0) {
+      for (int st = 0; st < kStages && st < lt; ++st) {
+        const int uses = (lt - 1 - st) / kStages + 1;  // tiles issued into stage st
+        mbar_drain(&s.full[st], (uses - 1) & 1, p.err);
+      }
+      for (int i = 0; i < 2; ++i)
+        if (q_issued[i] > 0) mbar_drain(&s.qfull[i], (q_issued[i] - 1) & 1, p.err);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
     // One thread: the per-tile loop carries no warp votes or warp barriers.

@@ -342,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ahead.valid()) ahead.next();
     int pages_next = chunk_pages(ahead);
     int lt = 0;  // local tile counter
+    int issued[kStages / kProducerWarps] = {};  // copies issued into this warp's stages
+    int q_issued[2] = {0, 0};                   // warp 0: Q loads issued into each slot
     bool new_group = true;
     while (cur.valid() && !*abort) {
       const int r0 = cur.row0();
@@ -363,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           mbar_arrive(&s.qfull[slot]);
         }
+        ++q_issued[slot];
       }
       const int npages_grp = div_up(cur.row_len(nr - 1), 64);
       const int tb = cur.tile_begin();
@@ -374,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (use > 0 && !mbar_wait_warp(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
         const int pid0 = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb));
         const int pid1 = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb) + 1);
+        ++issued[st / kProducerWarps];
         if (lane == 0) {
           const int pg1 = 2 * t + 1;
           const bool two = pg1 < npages_grp;
@@ -403,6 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         pages_next = chunk_pages(ahead);
       }
     }
+    // every copy this warp issued has landed before the CTA can exit (at once
+    // unless a wait ran out and the consumers stopped early)
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < kStages / kProducerWarps; ++i)
+        if (issued[i] > 0) mbar_drain(&s.full[warp + kProducerWarps * i], (issued[i] - 1) & 1, p.err);
+      for (int i = 0; i < 2; ++i)
+        if (q_issued[i] > 0) mbar_drain(&s.qfull[i], (q_issued[i] - 1) & 1, p.err);
+    }
+    __syncwarp();
   } else if (warp < kFirstEpiWarp) {
     // ---------------------------------------------------------- MMA issuers --
     // One thread per MMA warp: the per-tile loop is on the critical path of the

@@ -96,6 +96,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// Before a CTA exits, waits (bounded, whatever the abort flag says) for the
+// phase with the given parity, i.e. for copies this thread issued onto the
+// barrier to land: on the abort path (a wait that ran out) the consumers stop
+// waiting, but shared memory must outlive every copy still writing to it.
+// Gives up after 1e8 cycles (kErrTimeout).
+constexpr long long kDrainBudgetCycles = 100000000LL;
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kDrainBudgetCycles) {
+      raise_error(err, kErrTimeout);
+      return;
+    }
+  }
+}
+
 // mbar_wait taken by a whole warp: the result is the same in every lane, so a
 // warp that gives up does so together (no lane is left at a later __syncwarp
 // or warp-collective instruction).

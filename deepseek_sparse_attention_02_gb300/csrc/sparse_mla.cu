@@ -383,9 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // head's row of them into TMEM
       uint8_t* stage = msg0;  // 4 x 16 KB, 1024-aligned, within the two buffers
       if (leader) tma_prefetch_desc(&tm_q);
+      int q_rounds = 0;  // TMA rounds issued onto q_full
 #pragma unroll 1
       for (int rd = 0; rd < 3; ++rd) {
         const int c0 = 4 * rd, nc = rd < 2 ? 4 : 1;
+        ++q_rounds;
         if (leader) {
           mbar_arrive_expect_tx(&s.q_full, nc * kChunkBytes);
           for (int j = 0; j < nc; ++j)
@@ -411,6 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every thread has its rows before the buffers are refilled (or reused for P)
         if (named_bar_or(1, 128, !ok)) { bad = true; break; }
       }
+      // a round whose wait ran out may still be landing: it lands before the
+      // CTA can exit (at once on the normal path)
+      if (leader) mbar_drain(&s.q_full, (q_rounds - 1) & 1, p.err);
       tc_fence_before();
       __syncwarp();
       if (!bad && lane == 0) mbar_arrive(&s.q_ready);
