@@ -8,42 +8,48 @@
 // every selected latent crosses into the pair's shared memory once for S and
 // once for P V, and S is computed once:
 //
-//  CTA 0, the score CTA (TMEM: S tile [128 heads x 128 tokens] f32 at columns
-//  0-127, Q of the row at 128-415, lane = head, two bf16 per column):
+//  CTA 0, the score CTA (TMEM: two S tiles [128 heads x 128 tokens] f32 at
+//  columns 0-127 and 128-255, so S(i+1) is computed while the softmax reads
+//  S(i); elements 0-511 of Q at 256-511, lane = head, two bf16 per column; Q's
+//  rope elements 512-575 stay in shared memory as the A operand of the last
+//  K-chunk):
 //   warps 0-7  gather the nine [128 tokens x 64] K-chunks of each tile (16-byte
 //              cp.async, manual 128-byte swizzle, a skipped selection is
 //              zero-filled; completion by cp.async.mbarrier.arrive, so no
 //              gathering thread waits) into a 9-slot ring, one slot per chunk;
 //   warps 8-11 softmax, one thread per head: Q -> TMEM once (by TMA into
-//              the two idle message buffers, four 16 KB chunks at a time,
-//              then each thread moves its head's row; the gathers' cp.async
+//              the idle message buffer, two 16 KB chunks at a time, then
+//              each thread moves its head's row; the gathers' cp.async
 //              path is left to the gathers); per tile read
 //              S, mask skipped selections, keep a lazily moving reference (it
 //              moves only when a score exceeds it by more than 2^8), write P
 //              as bf16 into a K-major 128B-swizzled message buffer with the
-//              tile's O correction factors and running sums, and send the
-//              message to CTA 1 with one shared->shared bulk copy;
+//              tile's O correction factors and running sums (one local
+//              message buffer, rewritten once the copy has read it);
 //   warp 12    tcgen05 issuer of S = Q K^T (kind::f16, A = Q from TMEM,
-//              M = 128 heads, N = 128 tokens, K = 576).
+//              M = 128 heads, N = 128 tokens, K = 576);
+//   warp 13    sends each tile's message once the four softmax warps have
+//              written it, and frees the local buffer when the copy has read
+//              it, so the softmax warps never wait on the copy engine.
 //  CTA 1, the value CTA (TMEM: O [128 heads x 512] f32, all 512 columns):
 //   warps 0-7  gather the eight [128 tokens x 64] value chunks of each tile
 //              (the latent lines the score CTA read a tile earlier: L2 hits);
 //   warps 8-11 rescale O when a message says the reference moved, and write
 //              the normalised output at the end;
 //   warp 12    tcgen05 issuer of O += P V (A = P from the message, K-major;
-//              V MN-major from the ring, N = 128 per pair of chunks), whose
+//              V MN-major from the ring, N = 256 per four chunks), whose
 //              completion frees the message buffer in both CTAs (multicast
 //              commit) and the ring slots.
 // With more than one split the pair writes unnormalised partial O plus its
 // (max, sum) and a combine kernel merges them.
 //
-// The gathers set the pace: one SM takes in ~20 B/cycle of scattered 128-byte
-// lines by 16-byte cp.async, whatever the number of gathering warps or ring
-// slots and whether the lines are in L2 or in HBM (measured on GB300), so a
-// tile costs the score CTA ~7.8 k cycles for its 144 KB of K-chunks.  Two S
-// tiles in TMEM, a third of the chunks by TMA tile::gather4, and an L2
-// prefetch of whole latent rows were each measured against this design and
-// did not beat it.
+// Measured on GB300: one bf16 tcgen05.mma of M = 128, K = 16 holds the
+// tensor pipe ~105 cycles (~110 with A in TMEM) for any N <= 128 and ~128
+// cycles at N = 256, so P V issues N = 256; the 36 MMAs of one S tile
+// (N = 128, the tile's tokens) take ~4 k cycles, about what the score CTA's
+// 144 KB of gathers per tile take at the ~33 B/cycle one SM reaches with
+// 16-byte cp.async.  With one S tile the next tile's MMAs waited for the
+// softmax to read S (~7.8 k cycles per tile in all); with two they do not.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -58,7 +64,8 @@ namespace {
 constexpr int kGatherWarps = 8;
 constexpr int kSoftWarp = kGatherWarps;     // warps 8-11: softmax (CTA 0) / O warps (CTA 1)
 constexpr int kMmaWarp = kGatherWarps + 4;  // warp 12: MMA issuer; owns the TMEM allocation
-constexpr int kThreads = 32 * (kMmaWarp + 1);
+constexpr int kSendWarp = kMmaWarp + 1;     // warp 13: message sender (CTA 0)
+constexpr int kThreads = 32 * (kSendWarp + 1);
 constexpr int kTile = 128;
 constexpr int kChunksS = 9;  // 576 / 64: K-chunks per tile (score CTA)
 constexpr int kChunksV = 8;  // 512 / 64: value chunks per tile (value CTA)
@@ -72,8 +79,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // TMEM columns.
-constexpr uint32_t kSCol = 0;    // score CTA: S tile
-constexpr uint32_t kQCol = 128;  // score CTA: Q (288 columns)
+constexpr uint32_t kSCol = 0;    // score CTA: S tiles (2 x 128 columns)
+constexpr uint32_t kQCol = 256;  // score CTA: Q elements 0-511 (256 columns)
 constexpr uint32_t kTmemCols = 512;
 
 // Message score CTA -> value CTA for one tile: P [128 heads x 128 tokens] bf16
@@ -91,10 +98,12 @@ static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message layout");
 // multicast commit names a barrier by its offset), then each CTA's payload.
 struct Header {
   uint64_t full[kChunksS], empty[kChunksS];  // ring slots (one per chunk of a tile)
-  uint64_t s_full, s_free, q_ready;          // score CTA: S tile written / read, Q in TMEM
+  uint64_t s_full[2], s_free[2];             // score CTA: S tile b written / read
+  uint64_t q_ready;                          // score CTA: Q in TMEM
   uint64_t p_full[2], p_free[2];             // message buffer b: arrived / consumed by P V
   uint64_t need_fix, o_fixed, drain;         // value CTA: O rescale hand-off, final drain
   uint64_t q_full;                           // score CTA: a round of Q chunks landed
+  uint64_t msg_ready[2], msg_free[2];        // score CTA: message part written / read by its copy
   uint32_t tmem_base;
   int abort;
   int t_fix;  // tile whose P V waits for an O rescale, or -1 = no more tiles
@@ -103,9 +112,11 @@ constexpr uint32_t kHeaderBytes = 1024;
 static_assert(sizeof(Header) <= kHeaderBytes, "header");
 constexpr uint32_t kScoreRing = 0;
 constexpr uint32_t kScoreMsg = kChunksS * kChunkBytes;
+constexpr uint32_t kScoreRope = kScoreMsg + kMsgStride;  // Q elements 512-575, [128 x 64]
 constexpr uint32_t kValueMsg = 0;
 constexpr uint32_t kValueRing = 2 * kMsgStride;
-constexpr uint32_t kScorePayload = kScoreMsg + 2 * kMsgStride;
+constexpr uint32_t kScorePayload = kScoreRope + kChunkBytes;
+static_assert(kScoreRope % 1024 == 0, "128B-swizzled operands are 1024-byte aligned");
 constexpr uint32_t kValuePayload = kValueRing + kChunksV * kChunkBytes;
 constexpr uint32_t kPayloadBytes = kScorePayload > kValuePayload ? kScorePayload : kValuePayload;
 constexpr size_t kSmemBytes = 1024 + kHeaderBytes + kPayloadBytes;
@@ -136,8 +147,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 // 2^x by the hardware approximation (a few ulp; P is rounded to bf16 anyway).
 // 2^-inf = 0.
@@ -187,8 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.full[i], 32 * kGatherWarps);  // one cp.async completion per gather thread
       mbar_init(&s.empty[i], 1);                 // the MMA issuer's commit
     }
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.s_free, 4);   // the 4 softmax warps have read S
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.s_full[b], 1);
+      mbar_init(&s.s_free[b], 4);  // the 4 softmax warps have read S tile b
+    }
     mbar_init(&s.q_ready, 4);  // the 4 softmax warps have stored their Q rows
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.p_full[b], 1);  // the score CTA's remote arrive (+ the copy's bytes)
@@ -198,6 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.o_fixed, 4);
     mbar_init(&s.drain, 1);
     mbar_init(&s.q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.msg_ready[b], 4);  // the 4 softmax warps have written part b of the message
+      mbar_init(&s.msg_free[b], 1);   // the sender's copy has read part b
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
@@ -287,39 +302,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (rank == 0) {
       // ------------------------------------------------------ S MMA issuer --
-      // One thread; S(i) overwrites the S tile once the softmax has read S(i-1).
+      // One thread; S(i) goes to S tile i & 1 once the softmax has read S(i-2).
       constexpr uint32_t kIdescS = make_idesc(1, 1, 128, kTile, false, false);
-      const uint8_t* ring = pay + kScoreRing;
+      // The issuing thread shares its SM sub-partition with a softmax and two
+      // gather warps, so its loop is kept short: descriptors are the base
+      // ones plus constant offsets (the start-address field holds address
+      // >> 4 in 14 bits, and no operand ends above 256 KB, so adding to it
+      // never carries into the next field).
+      const uint64_t ring_desc = sw128_desc(smem_u32(pay + kScoreRing), 16, 1024);
+      const uint64_t rope_desc = sw128_desc(smem_u32(pay + kScoreRope), 16, 1024);
       if (lane == 0 && ntile > 0 && mbar_wait(&s.q_ready, 0, p.err, abort)) {
         tc_fence_after();
         for (int i = 0; i < ntile && !*abort; ++i) {
-          if (i > 0 && !mbar_wait(&s.s_free, (i - 1) & 1, p.err, abort)) break;
+          const int sb = i & 1;
+          if (i >= 2 && !mbar_wait(&s.s_free[sb], ((i - 2) >> 1) & 1, p.err, abort)) break;
           tc_fence_after();
+          const uint32_t d = tmem + kSCol + kTile * sb;
           bool bad = false;
+#pragma unroll
           for (int c = 0; c < kChunksS; ++c) {
             if (!mbar_wait(&s.full[c], i & 1, p.err, abort)) { bad = true; break; }
             fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor core
             tc_fence_after();
-            const uint32_t b0 = smem_u32(ring + c * kChunkBytes);
+            // chunk c of the ring; a K step of 16 elements is 32 bytes
+            const uint64_t bd = ring_desc + static_cast<uint64_t>(c * (kChunkBytes >> 4));
+            if (c < kChunksV) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ts(tmem + kSCol, tmem + kQCol + 32 * c + 8 * kk,
-                         sw128_desc(b0 + 32 * kk, 16, 1024), kIdescS, (c | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ts(d, tmem + kQCol + 32 * c + 8 * kk, bd + 2 * kk, kIdescS, (c | kk) != 0);
+            } else {
+              // the rope elements: A = Q's [128 x 64] rope chunk in shared memory
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) mma_f16(d, rope_desc + 2 * kk, bd + 2 * kk, kIdescS, 1u);
+            }
             mma_commit(&s.empty[c]);
           }
           if (bad) break;
-          mma_commit(&s.s_full);
+          mma_commit(&s.s_full[sb]);
         }
       }
       __syncwarp();
     } else {
       // ------------------------------------------------------ PV MMA issuer --
-      // O[:, 128 j2 .. +128] += P V_j2 per pair j2 of value chunks (N = 128);
-      // each pair's ring slots are freed as soon as its MMAs complete, so the
-      // next tile's gathers start while this tile's later pairs run.
-      constexpr uint32_t kIdescPV = make_idesc(1, 1, 128, 128, false, true);
+      // O[:, 256 j4 .. +256] += P V_j4 per four value chunks j4 (N = 256);
+      // each group's ring slots are freed as soon as its MMAs complete, so the
+      // next tile's gathers start while this tile's second group runs.
+      constexpr uint32_t kIdescPV = make_idesc(1, 1, 128, 256, false, true);
       const uint8_t* msg0 = pay + kValueMsg;
-      const uint8_t* ring = pay + kValueRing;
+      // as for S: base descriptors plus constant offsets (no carry out of the
+      // 14-bit start-address field below 256 KB)
+      const uint64_t v_desc = sw128_desc(smem_u32(pay + kValueRing), kChunkBytes, 1024);
       if (lane == 0) {
         int nfix = 0;
         for (int t = 0; t < ntile && !*abort; ++t) {
@@ -335,22 +367,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nfix;
           }
           bool bad = false;
-          const uint32_t pa = smem_u32(msg);
-          for (int j2 = 0; j2 < kChunksV / 2 && !bad; ++j2) {
-            for (int c = 2 * j2; c < 2 * j2 + 2; ++c)
+          const uint64_t p_desc = sw128_desc(smem_u32(msg), 16, 1024);
+#pragma unroll
+          for (int j4 = 0; j4 < kChunksV / 4; ++j4) {
+            for (int c = 4 * j4; c < 4 * j4 + 4; ++c)
               if (!mbar_wait(&s.full[c], t & 1, p.err, abort)) { bad = true; break; }
             if (bad) break;
             fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t v0 = smem_u32(ring + 2 * j2 * kChunkBytes);
-#pragma unroll 1
+            const uint64_t vd = v_desc + static_cast<uint64_t>(4 * j4 * (kChunkBytes >> 4));
+            // K step kk: tokens 16 kk .. +16, i.e. P chunk kk / 4 at byte 32 (kk % 4)
+            // and V rows 16 kk (2 KB further per step)
+#pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_f16(tmem + 128 * j2,
-                      sw128_desc(pa + (kk >> 2) * kChunkBytes + 32 * (kk & 3), 16, 1024),
-                      sw128_desc(v0 + 2048 * kk, kChunkBytes, 1024), kIdescPV,
+              mma_f16(tmem + 256 * j4,
+                      p_desc + static_cast<uint64_t>(((kk >> 2) * kChunkBytes + 32 * (kk & 3)) >> 4),
+                      vd + static_cast<uint64_t>((2048 * kk) >> 4), kIdescPV,
                       (t > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&s.empty[2 * j2]);
-            mma_commit(&s.empty[2 * j2 + 1]);
+            for (int c = 4 * j4; c < 4 * j4 + 4; ++c) mma_commit(&s.empty[c]);
           }
           if (bad) break;
           // message buffer b is free again in both CTAs once these MMAs complete
@@ -365,6 +399,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+  } else if (warp == kSendWarp) {
+    if (rank == 0 && lane == 0) {
+      // ---------------------------------------------------- message sender --
+      // Each message goes in two copies: part 0 (P of tokens 0-63) as soon as
+      // it is written, part 1 (P of tokens 64-127, the factors and sums) at
+      // the end of the tile; each part of the local buffer is freed when its
+      // copy has read it.
+      const uint32_t peer_msg0 = mapa_shared(smem_u32(pay + kValueMsg), 1);
+      const uint8_t* msg = pay + kScoreMsg;
+      int sent = 0;
+      for (int i = 0; i < ntile; ++i) {
+        const int b = i & 1;
+        if (!mbar_wait(&s.msg_ready[0], i & 1, p.err, abort)) break;
+        // the value CTA's buffer b is free once P V of tile i-2 has completed
+        if (i >= 2 && !mbar_wait_cluster(&s.p_free[b], ((i - 2) >> 1) & 1, p.err, abort)) break;
+        const uint32_t pbar = mapa_shared(smem_u32(&s.p_full[b]), 1);
+        const uint32_t dst = peer_msg0 + b * kMsgStride;
+        mbar_arrive_expect_tx_remote(pbar, kMsgBytes);
+        bulk_copy_s2s(dst, msg, kChunkBytes, pbar);
+        bulk_commit_group();
+        ++sent;
+        bulk_wait_group_read<0>();
+        mbar_arrive(&s.msg_free[0]);
+        if (!mbar_wait(&s.msg_ready[1], i & 1, p.err, abort)) break;
+        bulk_copy_s2s(dst + kChunkBytes, msg + kChunkBytes, kMsgBytes - kChunkBytes, pbar);
+        bulk_commit_group();
+        bulk_wait_group_read<0>();
+        mbar_arrive(&s.msg_free[1]);
+      }
+      bulk_wait_group<0>();
+      // the value CTA's last commits arrive here too: they land before the pair exits
+      for (int t = max(0, sent - 2); t < sent; ++t)
+        if (!mbar_wait_cluster(&s.p_free[t & 1], (t >> 1) & 1, p.err, abort)) break;
+    }
+    __syncwarp();
   } else if (rank == 0) {
     // ----------------------------------------------------------- softmax --
     const int quad = warp & 3;       // warps 8-11: TMEM lane quadrants 0-3
@@ -372,26 +441,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const bool leader = warp == kSoftWarp && lane == 0;
     uint8_t* msg0 = pay + kScoreMsg;
-    const uint32_t peer_msg0 = mapa_shared(smem_u32(pay + kValueMsg), 1);
     float m_run = -INFINITY, l_run = 0.f;
     bool bad = false;
     if (ntile > 0) {
-      // Q of the row -> TMEM columns [kQCol, kQCol + 288), lane h = head h,
-      // column j holding elements 2j (low half) and 2j + 1: in three rounds
-      // (chunks 0-3, 4-7, 8) TMA puts [128 heads x 64] K-chunks (128B-swizzled)
-      // into the message buffers, idle until tile 0, and each thread copies its
-      // head's row of them into TMEM
-      uint8_t* stage = msg0;  // 4 x 16 KB, 1024-aligned, within the two buffers
+      // Q elements 0-511 of the row -> TMEM columns [kQCol, kQCol + 256),
+      // lane h = head h, column j holding elements 2j (low half) and 2j + 1:
+      // in four rounds of two TMA boxes ([128 heads x 64] K-chunks,
+      // 128B-swizzled) into the message buffer, idle until tile 0, from which
+      // each thread copies its head's row into TMEM.  The first round also
+      // brings the rope chunk (elements 512-575) to its own shared memory.
+      uint8_t* stage = msg0;  // 2 x 16 KB, 1024-aligned, within the message buffer
       if (leader) tma_prefetch_desc(&tm_q);
       int q_rounds = 0;  // TMA rounds issued onto q_full
 #pragma unroll 1
-      for (int rd = 0; rd < 3; ++rd) {
-        const int c0 = 4 * rd, nc = rd < 2 ? 4 : 1;
+      for (int rd = 0; rd < kChunksV / 2; ++rd) {
+        const int c0 = 2 * rd, nc = 2;
         ++q_rounds;
         if (leader) {
-          mbar_arrive_expect_tx(&s.q_full, nc * kChunkBytes);
+          mbar_arrive_expect_tx(&s.q_full, (rd == 0 ? nc + 1 : nc) * kChunkBytes);
           for (int j = 0; j < nc; ++j)
             tma_load_2d(stage + j * kChunkBytes, &tm_q, &s.q_full, 64 * (c0 + j), row * kHeads);
+          if (rd == 0)
+            tma_load_2d(pay + kScoreRope, &tm_q, &s.q_full, 64 * kChunksV, row * kHeads);
         }
         __syncwarp();
         const bool ok = mbar_wait_warp(&s.q_full, rd & 1, p.err, abort);
@@ -425,7 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // valid if it is not -1 and its page is inside the cache: exactly the
     // selections the gather warps copy (the others are zero-filled there and
     // must get P = 0 here).  The indices are read two tiles ahead and their
-    // block-table entries one tile ahead.
+    // block-table entries one tile ahead, and compared only when the tile
+    // comes, so no load latency sits at the top of a tile.
     auto load_sel = [&](int i, int (&v)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -433,113 +505,113 @@ __global__ void __launch_bounds__(kThreads, 1)
         v[u] = (i < ntile && pos < s1) ? idx_row[pos] : -1;
       }
     };
-    auto sel_ok = [&](const int (&v)[4], bool (&ok)[4]) {
+    auto load_pg = [&](const int (&v)[4], int (&pg)[4]) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        ok[u] = false;
+        pg[u] = -1;
         const int64_t pg_i = v[u] / 64;
-        if (v[u] >= 0 && req >= 0 && pg_i < p.bt_stride) {
-          const int pg = p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i];
-          ok[u] = pg >= 0 && pg < p.num_pages;
-        }
+        if (v[u] >= 0 && req >= 0 && pg_i < p.bt_stride)
+          pg[u] = p.bt[static_cast<int64_t>(req) * p.bt_stride + pg_i];
       }
     };
-    int sel_next[4];
-    bool ok_cur[4];
-    {
-      int sel0[4];
-      load_sel(0, sel0);
-      load_sel(1, sel_next);
-      sel_ok(sel0, ok_cur);
-    }
+    int sel_cur[4], pg_cur[4], sel_next[4];
+    load_sel(0, sel_cur);
+    load_sel(1, sel_next);
+    load_pg(sel_cur, pg_cur);
+    bool msg_ok = true;  // the waits for the local message buffer
     for (int i = 0; i < ntile && !bad; ++i) {
       unsigned m[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) m[u] = __ballot_sync(0xffffffffu, ok_cur[u]);
-      {
-        int sel_after[4];
-        load_sel(i + 2, sel_after);
-        sel_ok(sel_next, ok_cur);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sel_next[u] = sel_after[u];
-      }
+      for (int u = 0; u < 4; ++u)
+        m[u] = __ballot_sync(0xffffffffu, sel_cur[u] >= 0 && pg_cur[u] >= 0 && pg_cur[u] < p.num_pages);
+      int sel_after[4], pg_next[4];
+      load_sel(i + 2, sel_after);
+      load_pg(sel_next, pg_next);
       const bool all_valid = (m[0] & m[1] & m[2] & m[3]) == 0xffffffffu;  // warp-uniform
-      const int b = i & 1;
-      uint8_t* msg = msg0 + b * kMsgStride;
-      const bool ok = mbar_wait_warp(&s.s_full, i & 1, p.err, abort);
+      const int b = i & 1;  // the value CTA's message buffer for this tile
+      uint8_t* msg = msg0;
+      const bool ok = mbar_wait_warp(&s.s_full[b], (i >> 1) & 1, p.err, abort);
       if (ok) tc_fence_after();
-      // message buffer b is rewritten only after the copy of tile i-2 has read it
-      if (leader && ok) bulk_wait_group_read<1>();
-      if (named_bar_or(1, 128, !ok)) { bad = true; break; }
-      // One pass over the tile's scores (log2 units, -inf if skipped), 64
-      // columns at a time.  P = 2^(x - m_t) against the running reference m_t,
-      // which only moves when a score exceeds it by more than the threshold
-      // (then P already written for this tile is brought to the new m_t).
-      float m_t = m_run, l_t = 0.f;
+      if (named_bar_or(1, 128, !ok || !msg_ok)) { bad = true; break; }
+      // Two passes over the tile's scores, 64 columns at a time.  First the
+      // tile's maximum (of the raw scores: the scale is positive, so scaling
+      // and rounding keep the order), then P = 2^(scale s - m_t) against the
+      // running reference m_t, which moves to the tile's maximum only when
+      // that exceeds it by more than the threshold (skipped selections give
+      // P = 0).  Knowing m_t before any P is written lets each half of P go
+      // to the value CTA as soon as it is written.
+      float hm_raw = -INFINITY;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         float v[64];
-        tmem_ld64_sync(lane_base + kSCol + 64 * half, v);
-        if (half == 1) {
-          // the whole S tile is in registers: S(i+1) may overwrite it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s.s_free);
-        }
+        tmem_ld64_sync(lane_base + kSCol + kTile * b + 64 * half, v);
         float h4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (all_valid) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            v[j] *= p.scale_log2;
-            h4[j & 3] = fmaxf(h4[j & 3], v[j]);
-          }
+          for (int j = 0; j < 64; ++j) h4[j & 3] = fmaxf(h4[j & 3], v[j]);
         } else {
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             const int t = 64 * half + j;
             const bool okj = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
-            v[j] = okj ? v[j] * p.scale_log2 : -INFINITY;
-            h4[j & 3] = fmaxf(h4[j & 3], v[j]);
+            h4[j & 3] = fmaxf(h4[j & 3], okj ? v[j] : -INFINITY);
           }
         }
-        const float hm = fmaxf(fmaxf(h4[0], h4[1]), fmaxf(h4[2], h4[3]));
-        const bool grow = hm > m_t + kRescaleThreshold || (m_t == -INFINITY && hm > -INFINITY);
-        if (grow) {
-          if (half == 1 && m_t > -INFINITY) {
-            // bring this head's P of tokens 0..63 (chunk 0) to the new reference
-            const float f = ex2_approx(m_t - hm);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              uint4* ptr = reinterpret_cast<uint4*>(msg + sw128_offset(h, q));
-              uint4 w = *ptr;
-              w.x = pack_bf16(bf16_lo(w.x) * f, bf16_hi(w.x) * f);
-              w.y = pack_bf16(bf16_lo(w.y) * f, bf16_hi(w.y) * f);
-              w.z = pack_bf16(bf16_lo(w.z) * f, bf16_hi(w.z) * f);
-              w.w = pack_bf16(bf16_lo(w.w) * f, bf16_hi(w.w) * f);
-              *ptr = w;
-            }
-            l_t *= f;
-          }
-          m_t = hm;
+        hm_raw = fmaxf(hm_raw, fmaxf(fmaxf(h4[0], h4[1]), fmaxf(h4[2], h4[3])));
+      }
+      const float hm = hm_raw * p.scale_log2;  // -inf if nothing of the tile is valid
+      float m_t = m_run, l_t = 0.f;
+      if (hm > m_t + kRescaleThreshold || (m_t == -INFINITY && hm > -INFINITY)) m_t = hm;
+      // m_t is -inf only while every score seen is -inf: those give P = 0
+      const float nref = m_t == -INFINITY ? 0.f : -m_t;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float v[64];
+        tmem_ld64_sync(lane_base + kSCol + kTile * b + 64 * half, v);
+        if (half == 1) {
+          // the S tile has been read: S(i+2) may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.s_free[b]);
         }
-        // m_t is -inf only while every score seen is -inf: those give P = 0
-        const float mref = m_t == -INFINITY ? 0.f : m_t;
         uint32_t pk[32];
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (all_valid) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float e0 = ex2_approx(v[2 * j] - mref);
-          const float e1 = ex2_approx(v[2 * j + 1] - mref);
-          pk[j] = pack_bf16(e0, e1);
-          l4[j & 3] += e0 + e1;  // the exact weights (P itself is rounded to bf16)
+          for (int j = 0; j < 32; ++j) {
+            const float e0 = ex2_approx(fmaf(v[2 * j], p.scale_log2, nref));
+            const float e1 = ex2_approx(fmaf(v[2 * j + 1], p.scale_log2, nref));
+            pk[j] = pack_bf16(e0, e1);
+            l4[j & 3] += e0 + e1;  // the exact weights (P itself is rounded to bf16)
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int t = 64 * half + 2 * j;
+            const bool ok0 = ((m[t >> 5] >> (t & 31)) & 1u) != 0;
+            const bool ok1 = ((m[(t + 1) >> 5] >> ((t + 1) & 31)) & 1u) != 0;
+            const float e0 = ok0 ? ex2_approx(fmaf(v[2 * j], p.scale_log2, nref)) : 0.f;
+            const float e1 = ok1 ? ex2_approx(fmaf(v[2 * j + 1], p.scale_log2, nref)) : 0.f;
+            pk[j] = pack_bf16(e0, e1);
+            l4[j & 3] += e0 + e1;
+          }
         }
         l_t += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        // part `half` of the local buffer is rewritten only after the copy of
+        // tile i-1 has read it (a wait that runs out stops the softmax at the
+        // next tile)
+        if (i > 0 && !mbar_wait_warp(&s.msg_free[half], (i - 1) & 1, p.err, abort)) msg_ok = false;
         // row h of chunk `half`: tokens 8q .. 8q+7 of the half in 16-byte piece q
         uint8_t* chunk = msg + half * kChunkBytes;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<uint4*>(chunk + sw128_offset(h, q)) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        if (half == 0) {
+          fence_proxy_async_smem();  // generic writes -> the bulk copy (async proxy)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.msg_ready[0]);
+        }
       }
       // O and l hold earlier tiles against m_run: they are brought to m_t
       const bool moved = m_t != m_run && m_run > -INFINITY;
@@ -551,25 +623,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool wmoved = __any_sync(0xffffffffu, moved);
       if (lane == 0) reinterpret_cast<uint32_t*>(msg + kMsgFlags)[quad] = wmoved ? 1u : 0u;
       fence_proxy_async_smem();  // generic writes -> the bulk copy (async proxy)
-      named_bar_sync(1, 128);
-      if (leader) {
-        // the value CTA's buffer b is free once P V of tile i-2 has completed
-        if (i < 2 || mbar_wait_cluster(&s.p_free[b], ((i - 2) >> 1) & 1, p.err, abort)) {
-          const uint32_t pbar = mapa_shared(smem_u32(&s.p_full[b]), 1);
-          mbar_arrive_expect_tx_remote(pbar, kMsgBytes);
-          bulk_copy_s2s(peer_msg0 + b * kMsgStride, msg, kMsgBytes, pbar);
-          bulk_commit_group();
-        }
-      }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&s.msg_ready[1]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        sel_cur[u] = sel_next[u];
+        pg_cur[u] = pg_next[u];
+        sel_next[u] = sel_after[u];
+      }
     }
-    if (leader) {
-      bulk_wait_group<0>();
-      // the value CTA's last commits arrive here too: they land before the pair exits
-      for (int t = max(0, ntile - 2); t < ntile && !bad; ++t)
-        if (!mbar_wait_cluster(&s.p_free[t & 1], (t >> 1) & 1, p.err, abort)) break;
-    }
-    __syncwarp();
+    if (!msg_ok) bad = true;
     if (!bad) {
       if (p.nsplit == 1) {
         if (p.lse)
