@@ -10,16 +10,18 @@
 // exclusive prefix over rows) that candidate_logits walks.
 //
 // candidate_logits: the indexer pipeline of indexer.cu over candidate
-// columns.  A tile is 128 sparse columns = two candidate blocks = two
-// 64-token pages, fetched by cp.async.bulk (4096 packed bytes + 256 scale
-// bytes each).  Converter warps expand e2m1 -> e4m3 (exact: every e2m1 value is
-// an e4m3 value) into a 128B-swizzled [128 x 128] tile with two byte-permute
-// lookups per 4 elements, and put each token's four UE8M0 scale bytes (one per
-// 32-element group) into a tensor-memory column.  The MMA warp then issues
-// four block-scaled kind::mxf8f6f4 MMAs (K = 32 each, the group g one taking
-// byte g of the token's scale word, the q side scaled by 2^0) into one
-// accumulator, so the tensor core applies the scales:
-//   logit = sum_h w'_h * ReLU(sum_g 2^(e_g - 127) * (k'_g . q'_g)[h]),
+// columns.  A tile is 128 sparse columns = two candidate blocks = two 64-token
+// pages.  The keys stay e2m1 all the way to the tensor core: a TMA tensor copy
+// whose element type is the 4-bit "16 values in 8 bytes, every 8 bytes padded
+// to 16" form writes each page's 64 keys into the 128B-swizzled shared-memory
+// layout in which the block-scaled kind::mxf8f6f4 MMA reads e2m1 operands
+// (one element per byte of footprint), and a bulk copy brings the page's 64 x 4
+// UE8M0 scale bytes.  Scale warps put each token's scale word into a
+// tensor-memory scale block; an MMA issuer issues four block-scaled MMAs (A =
+// keys e2m1, B = q e4m3, K = 32 each, group g taking byte g of the token's
+// scale word, the q side scaled by 2^0) into one accumulator, so the tensor
+// core applies the scales:
+//   logit = sum_h w'_h * ReLU(sum_g 2^(e_g - 127) * (k_g . q'_g)[h]),
 // and the epilogue is the dense indexer's (one accumulator, ReLU, weights).
 #include <cuda_bf16.h>
 
@@ -31,30 +33,45 @@
 namespace dsa {
 namespace {
 
-// warp 0 producer, warp 1 MMA issuer, warps 2-9 two converter groups (group
-// g converts the tiles == g mod 2, so two tiles are converted at once: one
-// group alone, converting a tile after the other, set the kernel's pace),
-// warps 10-13 the epilogue warpgroup (one accumulator per tile: light work)
-constexpr int kConvWarp = 2;
-constexpr int kFirstEpiWarp = 10;
-constexpr int kThreads = 32 * (kFirstEpiWarp + 4);
-constexpr int kStages = 8;  // raw (packed + scale) stages
-constexpr int kA = 4;       // converted e4m3 tiles (and their scale columns)
-static_assert(kA % 2 == 0 && kStages % 2 == 0,
-              "a stage and a converted slot always belong to the same converter group");
-constexpr int kAcc = 4;     // [128 x 64] accumulators; even: accumulator a is drained by warpgroup a % 2
+// Roles, each sized by measurement on GB300 (64 rows x 32768 columns per
+// layer: one producer warp 80 us, then 3 producers, 2 MMA issuers and 2
+// epilogue warpgroups 55 us; a warp's copies, and a lone issuing thread, are
+// slow enough to set the pace):
+//   warps 0-2   producers: warp w fills the stages of tiles == w (mod 3)
+//   warps 3-4   MMA issuers: warp 3 + i issues the tiles == i (mod 2)
+//   warps 5-8   scale warps (one per TMEM lane quadrant)
+//   warps 9-16  two epilogue warpgroups: group g drains the tiles == g (mod 2)
+constexpr int kProducers = 3;
+constexpr int kMmaWarp = kProducers;
+constexpr int kIssuers = 2;
+constexpr int kScaleWarp = kMmaWarp + kIssuers;
+constexpr int kFirstEpiWarp = kScaleWarp + 4;
+constexpr int kThreads = 32 * (kFirstEpiWarp + 8);
+constexpr int kStages = 12;  // key + scale stages
+constexpr int kAcc = 4;      // [128 x 64] accumulators
+// a stage is always filled by the same producer and issued by the same MMA
+// thread, and an accumulator always drained by the same epilogue group, so no
+// waiter ever looks at a barrier two phases ahead of it
+static_assert(kStages % kProducers == 0 && kStages % kIssuers == 0 && kAcc % 2 == 0 &&
+                  kAcc % kIssuers == 0,
+              "role / ring sizes");
 // Tensor-memory columns: the accumulators, then a 4-column scale block per
-// converted tile slot (row m of the tile: column m / 32, lane m % 32 in every
-// lane quadrant, byte g = the scale of its group g), then the q side's scale
-// block (every byte 2^0); each block 16-column aligned.
+// stage (row m of the tile: column m / 32, lane m % 32 in every lane quadrant,
+// byte g = the scale of its group g), then the q side's scale block (every
+// byte 2^0); each block 16-column aligned.
 constexpr uint32_t kSfaCol = 64 * kAcc;
 constexpr uint32_t kSfStride = 16;
-constexpr uint32_t kSfbCol = kSfaCol + kSfStride * kA;
+constexpr uint32_t kSfbCol = kSfaCol + kSfStride * kStages;
 constexpr uint32_t kOneScales = 0x7F7F7F7Fu;  // four UE8M0 bytes of 2^0
+constexpr uint32_t kFmtE2M1 = 5;              // instruction-descriptor code of e2m1
+constexpr uint32_t kKeyPageSmem = 64 * 128;   // a page's keys in shared memory (padded e2m1)
+// The tensor copy of 4-bit values completes its mbarrier transaction with the
+// packed byte count read from global memory (measured on GB300), not with the
+// padded bytes it writes.
+constexpr uint32_t kKeyPageTx = 64 * 64;
 constexpr int kTileCols = 128;
 constexpr int kChunkTiles = 4;
-constexpr uint32_t kPackedPage = 64 * 64;  // 4096
-constexpr uint32_t kSfPage = 64 * 4;       // 256
+constexpr uint32_t kSfPage = 64 * 4;  // a page's UE8M0 bytes
 
 __device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
 
@@ -179,7 +196,6 @@ struct CParams {
   float* logits;          // f32 output, or
   uint16_t* logits_bf16;  // bf16 output (round to nearest even) when not null
   int64_t ld;
-  int packed;             // each page's scales follow its keys (one copy per page)
   uint32_t* err;
 };
 
@@ -232,34 +248,22 @@ struct RowCursor {
 };
 
 struct CSmem {
-  uint8_t a[kA][128 * 128];          // converted e4m3 key tiles, K-major SW128
-  uint8_t q[2][64 * 128];            // q of the row, K-major SW128
-  // a stage's two pages: keys at raw + h * kPackedPage and scales at sf + h *
-  // kSfPage, or (pages with the scales right after the keys) the whole page at
-  // raw + h * (kPackedPage + kSfPage)
-  uint8_t raw[kStages][2 * (kPackedPage + kSfPage)];
-  uint8_t sf[kStages][2 * kSfPage];
+  uint8_t a[kStages][2 * kKeyPageSmem];  // a tile's keys, e2m1 padded, K-major SW128
+  uint8_t q[2][64 * 128];                // q of the row, K-major SW128
+  uint8_t sf[kStages][2 * kSfPage];      // a tile's 128 x 4 UE8M0 bytes
   float wq[2][64];
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kStages], empty[kStages], sready[kStages];
   uint64_t qfull[2], qempty[2];
-  uint64_t afull[kA], aempty[kA], tfull[kAcc], tempty[kAcc];
+  uint64_t tfull[kAcc], tempty[kAcc];
   uint32_t tmem_base;
   int abort;
 };
 
-// e2m1 magnitude code -> e4m3 byte: {0, 0.5, 1, 1.5 | 2, 3, 4, 6}
-constexpr uint32_t kLutLo = 0x3C383000u;
-constexpr uint32_t kLutHi = 0x4C484440u;
-
-// Four e2m1 nibbles (low 16 bits of x) -> four e4m3 bytes.
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t x) {
-  const uint32_t mag = __byte_perm(kLutLo, kLutHi, x & 0x7777u);
-  const uint32_t neg = __byte_perm(0u, 0xffffffffu, (x >> 1) & 0x4444u);
-  return mag | (neg & 0x80808080u);
-}
+static_assert(sizeof(CSmem) + 1024 <= 227 * 1024, "candidate shared memory exceeds 227 KB");
 
 __global__ void __launch_bounds__(kThreads, 1)
-    candidate_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const CParams p) {
+    candidate_logits_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k, const CParams p) {
   constexpr uint32_t kTmemCols = 512;  // accumulators + scale columns, rounded up to a power of 2
   static_assert(kSfbCol + 4 <= kTmemCols, "tensor-memory columns");
   extern __shared__ uint8_t smem_raw[];
@@ -273,15 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 4);  // the 4 warps of the converter group of the stage's tile
-    }
-    for (int i = 0; i < kA; ++i) {
-      mbar_init(&s.afull[i], 4);   // the 4 converter warps of the tile's group
-      mbar_init(&s.aempty[i], 1);  // the MMA commit
+      mbar_init(&s.empty[i], 1);   // the MMA commit
+      mbar_init(&s.sready[i], 4);  // the 4 scale warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.qfull[i], 32);
-      mbar_init(&s.qempty[i], 1 + 4);  // the MMA commit + the 4 epilogue warps
+      mbar_init(&s.qempty[i], kIssuers + 8);  // the MMA issuers' commits + the 8 epilogue warps
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -289,13 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   // the q side's scale block: every byte 2^0, in all 128 lanes (the four
   // epilogue warps cover the four lane quadrants)
-  if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4)
+  if (warp >= kFirstEpiWarp)
     tmem_st4_sync(s.tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfbCol,
                   kOneScales, kOneScales, kOneScales, kOneScales);
   tc_fence_before();
@@ -307,11 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c1 = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
   volatile int* abort = &s.abort;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer --
+  if (warp < kProducers) {
+    // ------------------------------------------------------------ producers --
+    const int pw = warp;  // fills the stages of tiles == pw (mod kProducers)
     RowCursor cur;
     cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
-    if (lane == 0) tma_prefetch_desc(&tm_q);
+    if (pw == 0 && lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+    }
     // The page of a tile column block takes two dependent loads (sparse
     // index, then block table).  Lane l holds block 2*tile_begin + l of a
     // chunk: its sparse index is loaded two chunks ahead and its page one chunk
@@ -338,11 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int blk2 = load_blk(ahead2);
     int pages1 = load_page(ahead1, blk1);
     int lt = 0, endr = 0;
-    int q_issued[2] = {0, 0};  // Q loads issued into each slot
+    int q_issued[2] = {0, 0};  // Q loads issued into each slot (producer 0)
+    int last_use[kStages / kProducers];  // phases issued into this producer's stages
+#pragma unroll
+    for (int i = 0; i < kStages / kProducers; ++i) last_use[i] = 0;
     bool new_group = true;
     while (cur.valid() && !*abort) {
       const int r = cur.row;
-      if (new_group) {
+      if (new_group && pw == 0) {
         const int slot = cur.gcount & 1;
         const int use = cur.gcount >> 1;
         if (use > 0 && !mbar_wait_warp(&s.qempty[slot], (use - 1) & 1, p.err, abort)) break;
@@ -360,42 +368,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tb = cur.tile_begin();
       bool bad = false;
       for (int t = tb; t < cur.tile_end(); ++t, ++lt) {
+        if (lt % kProducers != pw) continue;
         const int st = lt % kStages;
         const int use = lt / kStages;
         if (use > 0 && !mbar_wait_warp(&s.empty[st], (use - 1) & 1, p.err, abort)) { bad = true; break; }
+        last_use[st / kProducers] = use + 1;
         int pid[2];
         pid[0] = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb));
         pid[1] = __shfl_sync(0xffffffffu, pages_cur, 2 * (t - tb) + 1);
         const bool two = (2 * t + 1) * 64 < endr;
         if (lane == 0)
-          mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kPackedPage + kSfPage));
+          mbar_arrive_expect_tx(&s.full[st], (two ? 2u : 1u) * (kKeyPageTx + kSfPage));
         __syncwarp();
-        // the tile's copies go out from different lanes: one thread's bulk
-        // copies are taken one after another (~500 cycles each on GB300)
+        // the tile's copies go out from different lanes
         if (lane < 4) {
           const int h = lane >> 1;  // which page of the tile
-          const bool sf = (lane & 1) != 0;
           if (h == 0 || two) {
             int page = pid[h];
             if (page < 0 || page >= p.num_pages) {
-              if (!sf) raise_error(p.err, kErrBadPage);
+              if ((lane & 1) == 0) raise_error(p.err, kErrBadPage);
               page = 0;
             }
-            if (p.packed) {
-              // keys and scales contiguous: one copy of the page's 4352 bytes
-              if (!sf)
-                bulk_load_hint(s.raw[st] + h * (kPackedPage + kSfPage),
-                               p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride,
-                               kPackedPage + kSfPage, &s.full[st], evict_first);
-            } else if (!sf) {
-              bulk_load_hint(s.raw[st] + h * kPackedPage,
-                             p.k_fp4 + static_cast<int64_t>(page) * p.k_page_stride, kPackedPage,
-                             &s.full[st], evict_first);
-            } else {
+            if ((lane & 1) == 0)
+              tma_load_3d_hint(s.a[st] + h * kKeyPageSmem, &tm_k, &s.full[st], 0, 0, page,
+                               evict_first);
+            else
               bulk_load_hint(s.sf[st] + h * kSfPage,
                              p.k_sf + static_cast<int64_t>(page) * p.sf_page_stride, kSfPage,
                              &s.full[st], evict_first);
-            }
           }
         }
         __syncwarp();
@@ -410,47 +410,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       pages1 = load_page(ahead1, blk1);
     }
     // every copy issued has landed before the CTA can exit (at once unless a
-    // wait ran out and the consumers stopped early); tile i used stage i mod
-    // kStages, so the last lt tiles' phases are the ones to wait for
+    // wait ran out and the consumers stopped early)
     if (lane == 0) {
-      for (int st = 0; st < kStages && st < lt; ++st) {
-        const int uses = (lt - 1 - st) / kStages + 1;  // tiles issued into stage st
-        mbar_drain(&s.full[st], (uses - 1) & 1, p.err);
-      }
+#pragma unroll
+      for (int i = 0; i < kStages / kProducers; ++i)
+        if (last_use[i] > 0) mbar_drain(&s.full[kProducers * i + pw], (last_use[i] - 1) & 1, p.err);
       for (int i = 0; i < 2; ++i)
         if (q_issued[i] > 0) mbar_drain(&s.qfull[i], (q_issued[i] - 1) & 1, p.err);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp < kMmaWarp + kIssuers) {
     // ---------------------------------------------------------- MMA issuer --
-    // One thread: the per-tile loop carries no warp votes or warp barriers.
+    const int mi = warp - kMmaWarp;  // issues the tiles == mi (mod kIssuers)
+    // One thread; descriptors are the base ones plus constant offsets (the
+    // start-address field holds address >> 4; no operand ends above 256 KB,
+    // so adding to it never carries into the next field).
     if (lane == 0) {
       RowCursor cur;
       cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
+      const uint64_t ad0 = sw128_desc(smem_u32(s.a[0]), 16, 1024);
+      constexpr uint32_t kATileDesc = sizeof(s.a[0]) >> 4;
       int lt = 0;
       bool new_group = true;
       while (cur.valid() && !*abort) {
         const int slot = cur.gcount & 1;
         if (new_group && !mbar_wait(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) break;
         bool bad = false;
-        const uint32_t b0 = smem_u32(s.q[slot]);
+        const uint64_t bd = sw128_desc(smem_u32(s.q[slot]), 16, 1024);
         for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
-          const int ac = lt % kA;
+          if (lt % kIssuers != mi) continue;
+          const int st = lt % kStages;
           const int buf = lt % kAcc;
           const int ub = lt / kAcc;
-          if (!mbar_wait(&s.afull[ac], (lt / kA) & 1, p.err, abort)) { bad = true; break; }
+          // the scale warps have seen the stage land and filled its scale block
+          if (!mbar_wait(&s.sready[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
           if (ub > 0 && !mbar_wait(&s.tempty[buf], (ub - 1) & 1, p.err, abort)) { bad = true; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(s.a[ac]);
+          const uint64_t ad = ad0 + static_cast<uint64_t>(st * kATileDesc);
           const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * 64);
-          const uint32_t sfa = s.tmem_base + kSfaCol + kSfStride * static_cast<uint32_t>(ac);
+          const uint32_t sfa = s.tmem_base + kSfaCol + kSfStride * static_cast<uint32_t>(st);
           const uint32_t sfb = s.tmem_base + kSfbCol;
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            mma_mxf8f6f4_bs(d, sw128_desc(a0 + 32 * g, 16, 1024), sw128_desc(b0 + 32 * g, 16, 1024),
-                            make_idesc_bs(0, 0, 128, 64, static_cast<uint32_t>(g), 0u), sfa, sfb,
-                            g > 0 ? 1u : 0u);
-          mma_commit(&s.aempty[ac]);
+          // one K group of 32 elements is 32 bytes of footprint (2 in the address field)
+          mma_mxf8f6f4_bs(d, ad, bd, make_idesc_bs(kFmtE2M1, 0, 128, 64, 0u, 0u), sfa, sfb, 0u);
+          mma_mxf8f6f4_bs(d, ad + 2, bd + 2, make_idesc_bs(kFmtE2M1, 0, 128, 64, 1u, 0u), sfa, sfb, 1u);
+          mma_mxf8f6f4_bs(d, ad + 4, bd + 4, make_idesc_bs(kFmtE2M1, 0, 128, 64, 2u, 0u), sfa, sfb, 1u);
+          mma_mxf8f6f4_bs(d, ad + 6, bd + 6, make_idesc_bs(kFmtE2M1, 0, 128, 64, 3u, 0u), sfa, sfb, 1u);
+          mma_commit(&s.empty[st]);
           mma_commit(&s.tfull[buf]);
         }
         if (bad) break;
@@ -460,68 +465,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp < kFirstEpiWarp) {
-    // ---------------------------------------------------------- converters --
-    // A warp expands 8 token rows per step: lane l takes 16 packed bytes
-    // (piece l % 4 of row l / 4; a warp's loads are 512 contiguous bytes) and
-    // writes the 32 e4m3 bytes they expand to (two 16-byte chunks of the
-    // 128B-swizzled row; balanced over the banks).  Each warp also writes the
-    // slot's scale block into the TMEM lane quadrant it may access (warp % 4):
-    // lane l, columns j = 0..3 take the scale words of rows 32 j + l, so every
-    // quadrant holds the whole block.
-    const int cw = warp & 3;  // rows [32 cw, 32 cw + 32) of every tile
-    const int grp = (warp - kConvWarp) >> 2;  // converts the tiles == grp (mod 2)
-    const int key_stride = p.packed ? static_cast<int>(kPackedPage + kSfPage) : static_cast<int>(kPackedPage);
-    const int sf_stride = p.packed ? static_cast<int>(kPackedPage + kSfPage) : static_cast<int>(kSfPage);
-    const int piece = lane & 3;
+    // --------------------------------------------------------- scale warps --
+    // Each warp writes the stage's scale block into the TMEM lane quadrant it
+    // may access (warp % 4): lane l, columns j = 0..3 take the scale words of
+    // rows 32 j + l, so every quadrant holds the whole block.  The stage's
+    // scale block is free once its previous tile's MMAs completed, which its
+    // producer waited for before refilling the stage.
+    const int quad = warp & 3;
     RowCursor cur;
     cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
     int lt = 0;
     while (cur.valid() && !*abort) {
       bool bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
-        if ((lt & 1) != grp) continue;
         const int st = lt % kStages;
-        const int ac = lt % kA;
         if (!mbar_wait_warp(&s.full[st], (lt / kStages) & 1, p.err, abort)) { bad = true; break; }
-        if (lt >= kA && !mbar_wait_warp(&s.aempty[ac], ((lt / kA) - 1) & 1, p.err, abort)) { bad = true; break; }
-        uint8_t* dst = s.a[ac];
-        const uint8_t* sf_base = p.packed ? s.raw[st] + kPackedPage : s.sf[st];
+        uint32_t sfw[4];
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int tr = 32 * cw + 8 * it + (lane >> 2);
-          const uint4 v = *reinterpret_cast<const uint4*>(
-              s.raw[st] + (tr >> 6) * key_stride + (tr & 63) * 64 + 16 * piece);
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            o[2 * u] = e2m1x4_to_e4m3(in[u]);
-            o[2 * u + 1] = e2m1x4_to_e4m3(in[u] >> 16);
-          }
-          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * piece)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + sw128_offset(tr, 2 * piece + 1)) =
-              make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        {
-          uint32_t sfw[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int tr = 32 * j + lane;
-            sfw[j] = *reinterpret_cast<const uint32_t*>(sf_base + (tr >> 6) * sf_stride +
-                                                        (tr & 63) * 4);
-          }
-          tmem_st4_sync(s.tmem_base + (static_cast<uint32_t>(32 * cw) << 16) + kSfaCol +
-                            kSfStride * static_cast<uint32_t>(ac),
-                        sfw[0], sfw[1], sfw[2], sfw[3]);
-        }
-        fence_proxy_async_smem();  // generic-proxy writes of the tile -> tensor core
-        tc_fence_before();         // the scale column -> the MMA issuer
+        for (int j = 0; j < 4; ++j)
+          sfw[j] = *reinterpret_cast<const uint32_t*>(s.sf[st] + 128 * j + 4 * lane);
+        tmem_st4_sync(s.tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + kSfaCol +
+                          kSfStride * static_cast<uint32_t>(st),
+                      sfw[0], sfw[1], sfw[2], sfw[3]);
+        tc_fence_before();  // the scale block -> the MMA issuer
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&s.afull[ac]);
-          mbar_arrive(&s.empty[st]);
-        }
+        if (lane == 0) mbar_arrive(&s.sready[st]);
       }
       if (bad) break;
       cur.next();
@@ -529,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue --
     const int quad = warp & 3;
+    const int grp = (warp - kFirstEpiWarp) >> 2;  // drains the tiles == grp (mod 2)
     const int tr = quad * 32 + lane;  // token row of the tile == TMEM lane
     RowCursor cur;
     cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
@@ -539,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int endr = min(p.end[r], p.nb * 64);
       bool waited_q = false, bad = false;
       for (int t = cur.tile_begin(); t < cur.tile_end(); ++t, ++lt) {
+        if ((lt & 1) != grp) continue;
         if (!waited_q) {
           if (!mbar_wait_warp(&s.qfull[slot], (cur.gcount >> 1) & 1, p.err, abort)) { bad = true; break; }
           waited_q = true;
@@ -555,9 +525,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&s.tempty[buf]);
         // four partial sums: a single 64-long FMA chain is latency bound
         float a4[4] = {0.f, 0.f, 0.f, 0.f};
-        const float* wh = s.wq[slot];
+        const float4* wh = reinterpret_cast<const float4*>(s.wq[slot]);
 #pragma unroll
-        for (int h = 0; h < 64; ++h) a4[h & 3] = fmaf(wh[h], fmaxf(v[h], 0.f), a4[h & 3]);
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 w = wh[h4];
+          a4[0] = fmaf(w.x, fmaxf(v[4 * h4], 0.f), a4[0]);
+          a4[1] = fmaf(w.y, fmaxf(v[4 * h4 + 1], 0.f), a4[1]);
+          a4[2] = fmaf(w.z, fmaxf(v[4 * h4 + 2], 0.f), a4[2]);
+          a4[3] = fmaf(w.w, fmaxf(v[4 * h4 + 3], 0.f), a4[3]);
+        }
         const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
         const int col = t * kTileCols + tr;
         if (col < endr) {
@@ -582,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(s.tmem_base, kTmemCols);
   }
@@ -615,6 +591,17 @@ cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& d
                            msg_len))
       return cudaErrorInvalidValue;
   }
+  CUtensorMap tk;
+  {
+    // keys as [pages][64 tokens][128 e2m1] in the 4-bit "16 values in 8
+    // bytes, padded to 16 in shared memory" type; one box = one page, 128B swizzle
+    const uint64_t dims[3] = {128, 64, static_cast<uint64_t>(a.num_pages)};
+    const uint64_t strides[2] = {64, static_cast<uint64_t>(a.k_page_stride)};
+    const uint32_t box[3] = {128, 64, 1};
+    if (!encode_tensor_map(&tk, 2, 3, const_cast<uint8_t*>(a.k_fp4), dims, strides, box, true, msg,
+                           msg_len))
+      return cudaErrorInvalidValue;
+  }
   CParams p;
   p.q_scale = a.q_scale;
   p.w = a.w;
@@ -634,7 +621,6 @@ cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& d
   p.logits = a.logits;
   p.logits_bf16 = a.logits_bf16;
   p.ld = a.ld;
-  p.packed = (a.k_sf == a.k_fp4 + kPackedPage && a.sf_page_stride == a.k_page_stride) ? 1 : 0;
   p.err = dev.err_word;
   // at least 120 KB so that one CTA (holding all 512 TMEM columns) runs per SM
   const size_t smem = sizeof(CSmem) + 1024 > 120 * 1024 ? sizeof(CSmem) + 1024 : 120 * 1024;
@@ -642,7 +628,7 @@ cudaError_t launch_candidate_logits(const CandLogitsArgs& a, const DeviceInfo& d
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  candidate_logits_kernel<<<dev.sm_count, kThreads, smem, stream>>>(tq, p);
+  candidate_logits_kernel<<<dev.sm_count, kThreads, smem, stream>>>(tq, tk, p);
   return cudaGetLastError();
 }
 

@@ -99,8 +99,9 @@ bool encode_tensor_map(void* map_out, int dtype, int rank, void* base, const uin
     es[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
-  const CUtensorMapDataType dt =
-      dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = dtype == 0   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
   CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), dt, static_cast<cuuint32_t>(rank),
                         base, d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -223,12 +224,15 @@ dsa_status cand_logits_impl(const char* fn, const uint8_t* q_fp8, const float* q
     return fail(DSA_ERR_UNSUPPORTED,
                 "%s: the sparse block size must equal the %d-token page (got %d)", fn,
                 DSA_PAGE_TOKENS, block_size);
-  if (k_page_stride < 64 * 64 || k_page_stride % 16 || sf_page_stride < 256 ||
-      sf_page_stride % 16 || !aligned16(k_fp4) || !aligned16(k_sf) || !aligned16(q_fp8) ||
-      !aligned16(logits) || ld % 4 || ld < static_cast<int64_t>(nb) * block_size)
+  // the keys are read by a tensor copy of 4-bit elements: 32-byte aligned
+  // base and page stride
+  if (k_page_stride < 64 * 64 || k_page_stride % 32 || sf_page_stride < 256 ||
+      sf_page_stride % 16 || reinterpret_cast<uintptr_t>(k_fp4) % 32 || !aligned16(k_sf) ||
+      !aligned16(q_fp8) || !aligned16(logits) || ld % 4 ||
+      ld < static_cast<int64_t>(nb) * block_size)
     return fail(DSA_ERR_INVALID_ARG,
-                "%s: strides must be multiples of 16, buffers 16-byte aligned, ld >= nb*bs and "
-                "ld %% 4 == 0",
+                "%s: k_fp4 must be 32-byte aligned with k_page_stride %% 32 == 0, the other "
+                "strides multiples of 16, buffers 16-byte aligned, ld >= nb*bs and ld %% 4 == 0",
                 fn);
   const int64_t R64 = static_cast<int64_t>(num_req) * next_n;
   if (R64 > (1 << 20)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);

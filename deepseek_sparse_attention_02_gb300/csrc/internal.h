@@ -33,7 +33,9 @@ cudaError_t current_device_info(DeviceInfo* info);
 int set_last_error(int status, const char* msg);
 
 // Encodes a CUtensorMap through the driver entry point (no libcuda link).
-// dtype: 0 = uint8, 1 = bf16.  Returns false (and a message) on failure.
+// dtype: 0 = uint8, 1 = bf16, 2 = 4-bit values, 16 packed in 8 bytes in
+// global memory and padded to 16 bytes in shared memory (dims[0] counts the
+// 4-bit values).  Returns false (and a message) on failure.
 bool encode_tensor_map(void* map_out, int dtype, int rank, void* base, const uint64_t* dims,
                        const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128,
                        char* msg, size_t msg_len);

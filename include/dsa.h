@@ -313,8 +313,9 @@ dsa_status dsa_candidate_expand(const int32_t* cand, int R, int nb, int block_si
  * with k the MXFP4-dequantised key: e2m1 elements (element 2i in the low
  * nibble of byte i) times a UE8M0 scale 2^(e-127) per 32 elements.
  *
- *   k_fp4     device; page p's 64 keys (64 packed bytes each) at
- *             k_fp4 + p * k_page_stride bytes.
+ *   k_fp4     device, 32-byte aligned; page p's 64 keys (64 packed bytes
+ *             each) at k_fp4 + p * k_page_stride bytes (k_page_stride >= 4096,
+ *             a multiple of 32).
  *   k_sf      device; page p's 64 x 4 UE8M0 bytes (byte g of slot i scales
  *             elements 32g..32g+31) at k_sf + p * sf_page_stride bytes.
  *             (The canonical page is 4352 bytes: packed keys, then scales.)

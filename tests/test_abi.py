@@ -63,6 +63,15 @@ def test_host_validation_without_gpu(dsa):
     assert lib.dsa_indexer_logits(16, 16, 16, 16, 8448, 16, 8448, 1, 16, 1, 16, 0, 1, 16, 4,
                                   None) == 0
 
+    # candidate logits read the MXFP4 keys with a 4-bit tensor copy: k_fp4 must
+    # be 32-byte aligned and the key page stride a multiple of 32
+    cand = lambda k_fp4, stride: lib.dsa_candidate_logits(  # noqa: E731
+        64, 64, 64, k_fp4, stride, 64, 4352, 1, 64, 1, 0, 1, 64, 8, 64, 64, 64, 16, 64, 512, None)
+    assert cand(48, 4352) == 1
+    assert "32-byte" in dsa.dsa_last_error()
+    assert cand(64, 4368) == 1
+    assert cand(64, 4352) == 0  # no rows: nothing to do, no device needed
+
     # fused-histogram pair: hist is required and 16-byte aligned; the indexer
     # builds histograms for decode shapes only (next_n <= 2)
     assert lib.dsa_topk_hist(16, 2048, 16, 1, 8, None, 16, 0, None) == 1
