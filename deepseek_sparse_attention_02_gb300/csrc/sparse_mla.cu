@@ -18,9 +18,9 @@
 //              zero-filled; completion by cp.async.mbarrier.arrive, so no
 //              gathering thread waits) into a 9-slot ring, one slot per chunk;
 //   warps 8-11 softmax, one thread per head: Q -> TMEM once (by TMA into
-//              the idle message buffer, two 16 KB chunks at a time, then
-//              each thread moves its head's row; the gathers' cp.async
-//              path is left to the gathers); per tile read
+//              ring slots 0-7 before the gathers start, then each thread
+//              moves its head's row; the gathers' cp.async path is left to
+//              the gathers); per tile read
 //              S, mask skipped selections, keep a lazily moving reference (it
 //              moves only when a score exceeds it by more than 2^8), write P
 //              as bf16 into a K-major 128B-swizzled message buffer with the
@@ -268,6 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_toks(1, tk_next);
     }
     bool bad = false;
+    // the score CTA's ring holds Q's staging until Q is in TMEM
+    if (rank == 0 && ntile > 0 && !mbar_wait_warp(&s.q_ready, 0, p.err, abort)) bad = true;
     for (int i = 0; i < ntile && !bad; ++i) {
       // loads for the next tiles go out first; their results are used after
       // this tile's copies have been issued
@@ -446,16 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ntile > 0) {
       // Q elements 0-511 of the row -> TMEM columns [kQCol, kQCol + 256),
       // lane h = head h, column j holding elements 2j (low half) and 2j + 1:
-      // in four rounds of two TMA boxes ([128 heads x 64] K-chunks,
-      // 128B-swizzled) into the message buffer, idle until tile 0, from which
-      // each thread copies its head's row into TMEM.  The first round also
-      // brings the rope chunk (elements 512-575) to its own shared memory.
-      uint8_t* stage = msg0;  // 2 x 16 KB, 1024-aligned, within the message buffer
+      // one round of eight TMA boxes ([128 heads x 64] K-chunks, 128B-swizzled)
+      // into ring slots 0-7, from which each thread copies its head's row into
+      // TMEM; the gathers, whose first copies wait on two dependent index
+      // loads anyway, start filling the ring once Q is in TMEM (q_ready).  The
+      // round also brings the rope chunk (elements 512-575) to its own shared
+      // memory.
+      uint8_t* stage = pay + kScoreRing;  // 8 x 16 KB, 1024-aligned
       if (leader) tma_prefetch_desc(&tm_q);
       int q_rounds = 0;  // TMA rounds issued onto q_full
 #pragma unroll 1
-      for (int rd = 0; rd < kChunksV / 2; ++rd) {
-        const int c0 = 2 * rd, nc = 2;
+      for (int rd = 0; rd < 1; ++rd) {
+        const int c0 = 0, nc = kChunksV;
         ++q_rounds;
         if (leader) {
           mbar_arrive_expect_tx(&s.q_full, (rd == 0 ? nc + 1 : nc) * kChunkBytes);
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();  // these reads come before the next round's TMA writes
         }
-        // every thread has its rows before the buffers are refilled (or reused for P)
+        // every thread has its rows before the ring slots are refilled
         if (named_bar_or(1, 128, !ok)) { bad = true; break; }
       }
       // a round whose wait ran out may still be landing: it lands before the

@@ -199,3 +199,24 @@ def test_candidate_logits_split_key_and_scale_buffers():
     g, r = np_(got), np_(ref)
     for i in range(case.rows):
         assert np.array_equal(g[i, :E[i]].view(np.uint32), r[i, :E[i]].view(np.uint32)), i
+
+
+def test_candidate_logits_many_short_rows():
+    """Many rows of one or two tiles each, so every CTA walks several row
+    groups (the q slots are refilled after both MMA issuers and both epilogue
+    warpgroups have let go of them) and some rows have a partial last page;
+    MTP rows (next_n = 2) see different lengths of the same candidates."""
+    from deepseek_sparse_attention_02_gb300 import dsa
+    rng = np.random.default_rng(17)
+    ctx = [int(x) for x in rng.integers(70, 1100, size=190)]
+    next_n, nb = 2, 4
+    case = W.make_indexer_case(ctx, next_n=next_n, seed=17, device="cuda", fmt="mxfp4")
+    cand = W.make_candidates(ctx, next_n, 64, nb, seed=17, device="cuda")
+    si, end, sched, nbytes = expand(cand, case.layout.ctx_len, next_n)
+    ld = nb * 64
+    logits = cand_logits(case, si, end, sched, nbytes, ld)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error() == 0
+    assert case.rows > 2 * 152  # more row groups than CTAs
+    ref, mag = oracle_cand(case, si, end)
+    check_logits(np_(logits), ref, mag, np_(end))
