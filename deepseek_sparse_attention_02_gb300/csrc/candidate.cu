@@ -75,6 +75,25 @@ constexpr uint32_t kSfPage = 64 * 4;  // a page's UE8M0 bytes
 
 __device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
 
+// The row holding chunk c (sched[row] <= c < sched[row + 1]; sched is the
+// exclusive prefix of the rows' chunk counts, sched[R] > c), found by one
+// warp: each round the 32 lanes probe 32 evenly spaced rows, so R rows take
+// ceil(log32 R) dependent loads instead of log2 R.
+__device__ int find_row(const int32_t* sched, int R, int c) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = R;  // sched[lo] <= c < sched[hi]
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool le = idx < hi && sched[idx] <= c;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int j = 31 - __clz(m);  // lane 0 always qualifies (sched[lo] <= c)
+    lo = lo + j * step;
+    hi = min(hi, lo + step);
+  }
+  return lo;
+}
+
 // ------------------------------------------------------------- expansion --
 
 __global__ void __launch_bounds__(256) candidate_expand_kernel(CandExpandArgs a, uint32_t* err) {
@@ -210,8 +229,9 @@ struct RowCursor {
     tiles = div_up(min(end[row], max_cols), kTileCols);
     nchunk = div_up(tiles, kChunkTiles);
   }
+  // row0: the row of chunk c0 (find_row), or anything when c0 >= c1
   __device__ void init(const int32_t* sc, const int32_t* en, int nrows, int c0, int c1,
-                       int cols) {
+                       int cols, int row0) {
     max_cols = cols;
     sched = sc;
     end = en;
@@ -220,13 +240,7 @@ struct RowCursor {
     c_end = c1;
     gcount = 0;
     if (c >= c_end) return;
-    int lo = 0, hi = R;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sched[mid] <= c) lo = mid; else hi = mid;
-    }
-    row = lo;
-    while (sched[row + 1] <= c) ++row;
+    row = row0;
     enter();
     gchunk = c - sched[row];
   }
@@ -257,6 +271,7 @@ struct CSmem {
   uint64_t tfull[kAcc], tempty[kAcc];
   uint32_t tmem_base;
   int abort;
+  int row0;  // the row of this CTA's first chunk
 };
 
 static_assert(sizeof(CSmem) + 1024 <= 227 * 1024, "candidate shared memory exceeds 227 KB");
@@ -307,12 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c0 = static_cast<int>((static_cast<long long>(total) * blockIdx.x) / gridDim.x);
   const int c1 = static_cast<int>((static_cast<long long>(total) * (blockIdx.x + 1)) / gridDim.x);
   volatile int* abort = &s.abort;
+  if (warp == 0 && c0 < c1) {
+    const int r = find_row(p.sched, p.R, c0);
+    if (lane == 0) s.row0 = r;
+  }
+  __syncthreads();
+  const int row0 = s.row0;
 
   if (warp < kProducers) {
     // ------------------------------------------------------------ producers --
     const int pw = warp;  // fills the stages of tiles == pw (mod kProducers)
     RowCursor cur;
-    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
+    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64, row0);
     if (pw == 0 && lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -427,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so adding to it never carries into the next field).
     if (lane == 0) {
       RowCursor cur;
-      cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
+      cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64, row0);
       const uint64_t ad0 = sw128_desc(smem_u32(s.a[0]), 16, 1024);
       constexpr uint32_t kATileDesc = sizeof(s.a[0]) >> 4;
       int lt = 0;
@@ -473,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // producer waited for before refilling the stage.
     const int quad = warp & 3;
     RowCursor cur;
-    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
+    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64, row0);
     int lt = 0;
     while (cur.valid() && !*abort) {
       bool bad = false;
@@ -500,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = (warp - kFirstEpiWarp) >> 2;  // drains the tiles == grp (mod 2)
     const int tr = quad * 32 + lane;  // token row of the tile == TMEM lane
     RowCursor cur;
-    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64);
+    cur.init(p.sched, p.end, p.R, c0, c1, p.nb * 64, row0);
     int lt = 0;
     while (cur.valid() && !*abort) {
       const int slot = cur.gcount & 1;
