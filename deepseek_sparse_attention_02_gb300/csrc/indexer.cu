@@ -230,6 +230,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // The barriers and TMEM are set up before the wait for the previous kernel
+  // (no global memory is touched until the wait).
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 4);  // the 4 epilogue warps of the tile (after tfull, so the MMA is done)
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);  // the 4 warps of the warpgroup that drains accumulator i
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.qfull[i], 32);     // the 32 lanes of producer warp 0 (w*sq) + TMA bytes
+      mbar_init(&s.qempty[i], kMmaWarps + 8); // MMA commits + 8 epilogue warps
+    }
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
   pdl_launch_dependents_and_wait();
 
   // ---- per-request chunk counts and their exclusive prefix (all threads) ----
@@ -288,22 +306,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 4);  // the 4 epilogue warps of the tile (after tfull, so the MMA is done)
-    }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);  // the 4 warps of the warpgroup that drains accumulator i
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.qfull[i], 32);     // the 32 lanes of producer warp 0 (w*sq) + TMA bytes
-      mbar_init(&s.qempty[i], kMmaWarps + 8); // MMA commits + 8 epilogue warps
-    }
-    fence_mbar_init();
-  }
-  if (warp == kMmaWarp) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

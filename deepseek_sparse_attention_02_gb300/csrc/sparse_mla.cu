@@ -175,20 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t rank = cluster_ctarank();  // 0 = score CTA, 1 = value CTA
-  pdl_launch_dependents_and_wait();
-  const int row = blockIdx.x >> 1;
-  const int split = blockIdx.y;
-  // the block-table row of this query row (an out-of-range one reads nothing)
-  int req = p.row_bt ? p.row_bt[row] : row / p.next_n;
-  if (p.row_bt && (req < 0 || req >= p.bt_num_rows)) {
-    if (tid == 0 && rank == 0) raise_error(p.err, kErrBadPage);
-    req = -1;
-  }
-  const int s0 = split * p.tokens_per_split;
-  const int s1 = min(p.k, s0 + p.tokens_per_split);
-  const int ntile = s1 > s0 ? (s1 - s0 + kTile - 1) / kTile : 0;
-  const int32_t* idx_row = p.idx + static_cast<int64_t>(row) * p.k;
-
+  // The setup reads no global memory, so it runs before the wait for the
+  // previous kernel: barriers, TMEM, the pair's first cluster barrier.
   if (tid == 0) {
     s.abort = 0;
     s.t_fix = 0;
@@ -220,6 +208,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // both CTAs' barriers are initialised before any remote arrival or copy
   cluster_sync_all();
   tc_fence_after();
+  pdl_launch_dependents_and_wait();
+  const int row = blockIdx.x >> 1;
+  const int split = blockIdx.y;
+  // the block-table row of this query row (an out-of-range one reads nothing)
+  int req = p.row_bt ? p.row_bt[row] : row / p.next_n;
+  if (p.row_bt && (req < 0 || req >= p.bt_num_rows)) {
+    if (tid == 0 && rank == 0) raise_error(p.err, kErrBadPage);
+    req = -1;
+  }
+  const int s0 = split * p.tokens_per_split;
+  const int s1 = min(p.k, s0 + p.tokens_per_split);
+  const int ntile = s1 > s0 ? (s1 - s0 + kTile - 1) / kTile : 0;
+  const int32_t* idx_row = p.idx + static_cast<int64_t>(row) * p.k;
+
   volatile int* abort = &s.abort;
   const uint32_t tmem = s.tmem_base;
 
