@@ -406,8 +406,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // scheduled from now on; and this kernel waits here until the kernel before
 // it has completed and its memory is visible (at once if it was launched
 // without the attribute).  Every kernel of the library calls both before its
-// first global memory access, so only launch latency and CTA placement
-// overlap the previous kernel.
+// first global memory access, so only launch latency, CTA placement and
+// on-chip setup (mbarriers, TMEM) overlap the previous kernel.
 __device__ __forceinline__ void pdl_launch_dependents_and_wait() {
   asm volatile("griddepcontrol.launch_dependents;\n\tgriddepcontrol.wait;" ::: "memory");
 }
