@@ -34,16 +34,16 @@ namespace dsa {
 namespace {
 
 // Roles, each sized by measurement on GB300 (64 rows x 32768 columns per
-// layer: one producer warp 80 us, then 3 producers, 2 MMA issuers and 2
-// epilogue warpgroups 55 us; a warp's copies, and a lone issuing thread, are
-// slow enough to set the pace):
-//   warps 0-2   producers: warp w fills the stages of tiles == w (mod 3)
-//   warps 3-4   MMA issuers: warp 3 + i issues the tiles == i (mod 2)
-//   warps 5-8   scale warps (one per TMEM lane quadrant)
-//   warps 9-16  two epilogue warpgroups: group g drains the tiles == g (mod 2)
-constexpr int kProducers = 3;
+// layer: one producer warp, one issuer and one epilogue warpgroup 69.9 us;
+// 3 producers, 2 issuers and 2 epilogue warpgroups 55 us; 4 and 4 54 us: a
+// warp's copies, and a lone issuing thread, are slow enough to set the pace):
+//   warps 0-3   producers: warp w fills the stages of tiles == w (mod 4)
+//   warps 4-7   MMA issuers: warp 4 + i issues the tiles == i (mod 4)
+//   warps 8-11  scale warps (one per TMEM lane quadrant)
+//   warps 12-19 two epilogue warpgroups: group g drains the tiles == g (mod 2)
+constexpr int kProducers = 4;
 constexpr int kMmaWarp = kProducers;
-constexpr int kIssuers = 2;
+constexpr int kIssuers = 4;
 constexpr int kScaleWarp = kMmaWarp + kIssuers;
 constexpr int kFirstEpiWarp = kScaleWarp + 4;
 constexpr int kThreads = 32 * (kFirstEpiWarp + 8);
