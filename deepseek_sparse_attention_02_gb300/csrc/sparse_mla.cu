@@ -20,8 +20,8 @@
 //   warps 8-11 softmax, one thread per head: Q -> TMEM once (by TMA into
 //              ring slots 0-7 before the gathers start, then each thread
 //              moves its head's row; the gathers' cp.async path is left to
-//              the gathers); per tile read
-//              S, mask skipped selections, keep a lazily moving reference (it
+//              the gathers); per tile read S twice (its maximum, then P),
+//              mask skipped selections, keep a lazily moving reference (it
 //              moves only when a score exceeds it by more than 2^8), write P
 //              as bf16 into a K-major 128B-swizzled message buffer with the
 //              tile's O correction factors and running sums (one local
@@ -43,13 +43,14 @@
 // With more than one split the pair writes unnormalised partial O plus its
 // (max, sum) and a combine kernel merges them.
 //
-// Measured on GB300: one bf16 tcgen05.mma of M = 128, K = 16 holds the
-// tensor pipe ~105 cycles (~110 with A in TMEM) for any N <= 128 and ~128
-// cycles at N = 256, so P V issues N = 256; the 36 MMAs of one S tile
-// (N = 128, the tile's tokens) take ~4 k cycles, about what the score CTA's
-// 144 KB of gathers per tile take at the ~33 B/cycle one SM reaches with
-// 16-byte cp.async.  With one S tile the next tile's MMAs waited for the
-// softmax to read S (~7.8 k cycles per tile in all); with two they do not.
+// Measured on GB300: a lone thread issuing bf16 MMAs (M = 128, K = 16) in a
+// tight loop is held 64 cycles per MMA for N <= 128 and 128 at N = 256 (so
+// P V issues N = 256), and every instruction between its MMAs adds to that,
+// hence descriptors formed as base + constant offset.  A tile then costs the
+// score CTA ~6 k cycles at the ~1.6 GHz the SMs run at during this kernel in
+// the decode step: its 144 KB of 16-byte gathers (~24.5 B/cycle per SM), with
+// the S / softmax / P V chain close behind.  With one S tile the next tile's
+// MMAs waited for the softmax to read S; with two they do not.
 #include <cuda_bf16.h>
 
 #include <cmath>
