@@ -357,18 +357,13 @@ __device__ uint64_t radix_select(const Src& src, uint32_t need, Sel st, TkSmem& 
 }
 
 // Cutoff estimate: the lower edge of the 12-bit key prefix (sign, exponent,
-// 3 mantissa bits) bin that holds the q-th largest of the n sample keys, from
-// one 4096-bin histogram in `bins` (shared memory) and a block scan from the
+// 3 mantissa bits) bin that holds the q-th largest of the sample keys, from
+// their 4096-bin histogram in `bins` (shared memory) and a block scan from the
 // top bin down.  Keeping every key >= that edge keeps at least q / n of the
-// row in expectation.
-__device__ uint32_t local_tau(const uint32_t* sample, int n, uint32_t q, uint32_t* bins,
-                              TkSmem& s) {
+// row (n keys sampled) in expectation.
+__device__ uint32_t tau_from_bins(uint32_t q, const uint32_t* bins, TkSmem& s) {
   constexpr int kTauBins = 4096, kPer = kTauBins / kT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kTauBins; i += kT) bins[i] = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += kT) atomicAdd(&bins[sample[i] >> 20], 1u);
-  __syncthreads();
   // thread t owns bins [kTauBins - kPer*(t+1), kTauBins - kPer*t), walked downwards
   const int top = kTauBins - kPer * tid - 1;
   uint32_t sum = 0;
@@ -684,27 +679,35 @@ __global__ void __launch_bounds__(kT, 1) topk_kernel(const TkParams p) {
       uint32_t tau = 0;
       const bool exact = hrow && hist_tau(hrow, L, static_cast<uint32_t>(p.k), s, &tau);
       if (!exact) {
-        int ns;
+        // The sample's keys go straight from the loads into the cutoff
+        // histogram (its bins are cleared while the loads are in flight).
+        constexpr int kTauBins = 4096;
+        const int ns = L >= kSample ? kSample : L;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (L >= kSample && tid < kSample / 4) {
+          // float4 tid of the sample: group tid / 2, half tid % 2
+          const int64_t g0 =
+              ((static_cast<int64_t>(tid >> 1) * (L - 8)) / (kGroups - 1)) & ~3ll;
+          v = rowp.load4(g0 + 4 * (tid & 1));
+        }
+        for (int i = tid; i < kTauBins; i += kT) s.tau_bins[i] = 0;
+        __syncthreads();
         if (L >= kSample) {
-          ns = kSample;
           if (tid < kSample / 4) {
-            // float4 tid of the sample: group tid / 2, half tid % 2
-            const int64_t g0 =
-                ((static_cast<int64_t>(tid >> 1) * (L - 8)) / (kGroups - 1)) & ~3ll;
-            const float4 v = rowp.load4(g0 + 4 * (tid & 1));
-            *reinterpret_cast<uint4*>(s.sample + 4 * tid) =
-                make_uint4(key_of(v.x), key_of(v.y), key_of(v.z), key_of(v.w));
+            atomicAdd(&s.tau_bins[key_of(v.x) >> 20], 1u);
+            atomicAdd(&s.tau_bins[key_of(v.y) >> 20], 1u);
+            atomicAdd(&s.tau_bins[key_of(v.z) >> 20], 1u);
+            atomicAdd(&s.tau_bins[key_of(v.w) >> 20], 1u);
           }
         } else {
-          ns = L;
-          for (int i = tid; i < L; i += kT) s.sample[i] = key_of(rowp.load1(i));
+          for (int i = tid; i < L; i += kT) atomicAdd(&s.tau_bins[key_of(rowp.load1(i)) >> 20], 1u);
         }
         __syncthreads();
         // q = ceil(2k ns / L) sample keys above tau (integer arithmetic: FP64 is
         // a slow pipe on GB300 and every thread evaluates this)
         const int64_t want = (2 * static_cast<int64_t>(p.k) * ns + L - 1) / L;
         const uint32_t q = static_cast<uint32_t>(want < ns ? want : ns);
-        tau = local_tau(s.sample, ns, q > 0 ? q : 1u, s.tau_bins, s);
+        tau = tau_from_bins(q > 0 ? q : 1u, s.tau_bins, s);
       }
       // 2. one streaming pass: compact the survivors (key >= tau); with two
       // CTAs, columns [0, h) and [h, L), h a multiple of 4 (16-byte loads)
