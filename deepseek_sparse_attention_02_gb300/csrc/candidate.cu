@@ -265,7 +265,7 @@ struct CSmem {
   uint8_t a[kStages][2 * kKeyPageSmem];  // a tile's keys, e2m1 padded, K-major SW128
   uint8_t q[2][64 * 128];                // q of the row, K-major SW128
   uint8_t sf[kStages][2 * kSfPage];      // a tile's 128 x 4 UE8M0 bytes
-  float wq[2][64];
+  alignas(16) float wq[2][64];
   uint64_t full[kStages], empty[kStages], sready[kStages];
   uint64_t qfull[2], qempty[2];
   uint64_t tfull[kAcc], tempty[kAcc];
@@ -544,18 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.tempty[buf]);
-        // four partial sums: a single 64-long FMA chain is latency bound
-        float a4[4] = {0.f, 0.f, 0.f, 0.f};
-        const float4* wh = reinterpret_cast<const float4*>(s.wq[slot]);
-#pragma unroll
-        for (int h4 = 0; h4 < 16; ++h4) {
-          const float4 w = wh[h4];
-          a4[0] = fmaf(w.x, fmaxf(v[4 * h4], 0.f), a4[0]);
-          a4[1] = fmaf(w.y, fmaxf(v[4 * h4 + 1], 0.f), a4[1]);
-          a4[2] = fmaf(w.z, fmaxf(v[4 * h4 + 2], 0.f), a4[2]);
-          a4[3] = fmaf(w.w, fmaxf(v[4 * h4 + 3], 0.f), a4[3]);
-        }
-        const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+        const float acc = relu_dot64(v, s.wq[slot]);
         const int col = t * kTileCols + tr;
         if (col < endr) {
           const int64_t o = static_cast<int64_t>(r) * p.ld + col;

@@ -202,7 +202,7 @@ struct Smem {
   uint8_t keys[kStages][kStageBytes];  // 1024-aligned stage tiles
   uint8_t q[2][kQBytes];
   float scales[kStages][kTileTokens];
-  float wq[2][N];
+  alignas(16) float wq[2][N];
   int prefix[kMaxReq + 1];
   uint64_t full[kStages], empty[kStages];
   uint64_t qfull[2], qempty[2];
@@ -495,12 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < G; ++j) {
           float v[64];
           tmem_ld64_sync(taddr + j * 64, v);
-          // four partial sums: a single 64-long FMA chain is latency bound
-          float a4[4] = {0.f, 0.f, 0.f, 0.f};
-          const float* wj = s.wq[slot] + j * 64;
-#pragma unroll
-          for (int h = 0; h < 64; ++h) a4[h & 3] = fmaf(wj[h], fmaxf(v[h], 0.f), a4[h & 3]);
-          const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+          const float acc = relu_dot64(v, s.wq[slot] + j * 64);
           if (j < nr && tok < cur.row_len(j) && tok < p.ld)
             p.logits[static_cast<int64_t>(r0 + j) * p.ld + tok] = acc * sc;
         }
@@ -559,12 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < G; ++j) {
           float v[64];
           tmem_ld64_sync(taddr + j * 64, v);
-          // four partial sums: a single 64-long FMA chain is latency bound
-          float a4[4] = {0.f, 0.f, 0.f, 0.f};
-          const float* wj = s.wq[slot] + j * 64;
-#pragma unroll
-          for (int h = 0; h < 64; ++h) a4[h & 3] = fmaf(wj[h], fmaxf(v[h], 0.f), a4[h & 3]);
-          const float acc = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+          const float acc = relu_dot64(v, s.wq[slot] + j * 64);
           if (j < nr && tok < cur.row_len(j) && tok < p.ld) {
             const float logit = acc * sc;
             p.logits[static_cast<int64_t>(r0 + j) * p.ld + tok] = logit;

@@ -507,6 +507,40 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// ------------------------------------------------------ packed f32 math --
+// d = a * b + c on two f32 lanes at once (fma.rn.f32x2): each lane rounds
+// exactly as fmaf does, so results are bit-identical to two fmaf calls.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// sum_h w[h] * max(d[h], 0) over the 64 heads of one query row (the
+// indexer's head reduction), in four partial sums over h mod 4 (a single
+// 64-long chain is latency bound) added as (s0 + s1) + (s2 + s3); w is
+// 16-byte aligned.  The four sums run as two packed pairs.
+__device__ __forceinline__ float relu_dot64(const float (&d)[64], const float* w) {
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int h4 = 0; h4 < 16; ++h4) {
+    const float4 ww = w4[h4];
+    s01 = fma2(make_float2(ww.x, ww.y),
+               make_float2(fmaxf(d[4 * h4], 0.f), fmaxf(d[4 * h4 + 1], 0.f)), s01);
+    s23 = fma2(make_float2(ww.z, ww.w),
+               make_float2(fmaxf(d[4 * h4 + 2], 0.f), fmaxf(d[4 * h4 + 3], 0.f)), s23);
+  }
+  return (s01.x + s01.y) + (s23.x + s23.y);
+}
+
 // mbar_wait with cluster-scope acquire (same budget and abort rule).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* err,
                                                   volatile int* abort) {
