@@ -42,10 +42,11 @@ sys.path.insert(0, ROOT)
 
 # DRAM bytes (read + write) of one dsa_indexer_logits launch per cached token,
 # measured by ncu on this workload at 16 requests x 131072 tokens, next_n = 2
-# (`bench.py --requests 16 --no-candidate --no-layers --no-prefill
-# --no-cpu-baseline --steps 1 --warmup 1`, fourth indexer launch): 277.29 MB
-# read + 6.66 MB written (the rest of the logits leave L2 after the kernel).
-INDEXER_DRAM_BYTES_PER_TOKEN = (277.29e6 + 6.66e6) / (16 * 131072)
+# (`bench.py --requests 16 --no-candidate --no-layers --no-prefill --no-configs
+# --no-cpu-baseline --steps 1 --warmup 3`, fourth indexer launch, the current
+# kernel): 277.30 MB read + 6.76 MB written (the rest of the logits leave L2
+# after the kernel).
+INDEXER_DRAM_BYTES_PER_TOKEN = (277.30e6 + 6.76e6) / (16 * 131072)
 METRIC = "indexer keys scored/s + HBM GB/s at 128K decode; top-k rows/s; sparse-attn tok/s"
 WORKLOAD = ("128K MTP decode: 32 requests x 131072 ctx, next_n=2 (64 rows), FP8 indexer "
             "64x128 over 64-token shuffled pages, exact top-2048, sparse MLA 128 heads x "
