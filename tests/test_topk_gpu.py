@@ -52,6 +52,41 @@ def test_topk_all_equal_takes_exact_fallback():
     assert dsa.dsa_get_device_error(clear=True) == dsa.DEVERR_CAPACITY
 
 
+def _sample_positions(L):
+    """The columns the long-row path samples for its cutoff: 256 runs of 8
+    consecutive scores, run i starting at (i (L - 8) / 255) rounded down to a
+    multiple of 4 (16-byte loads)."""
+    pos = []
+    for i in range(256):
+        g0 = ((i * (L - 8)) // 255) & ~3
+        pos.extend(range(g0, g0 + 8))
+    return pos
+
+
+@pytest.mark.parametrize("Lr", [131072, 65536])
+def test_topk_sample_overestimate_takes_exact_redo(Lr):
+    """A row whose sampled columns hold its 2048 largest scores, spread over
+    ten octaves (80 bins of the 12-bit key prefix the cutoff is read from):
+    the cutoff estimated from the sample keeps only about 2k * 2048 / L of
+    them, fewer than k, so the row is redone by the exact full-row select; the
+    result is still exact and the device error word reports the missed
+    estimate.  131072 columns run on a CTA pair, 65536 on one CTA."""
+    from deepseek_sparse_attention_02_gb300 import dsa
+    dsa.dsa_get_device_error(clear=True)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    logits = torch.randn(1, Lr, generator=g, device="cuda")  # all below 8
+    pos = _sample_positions(Lr)
+    assert len(set(pos)) == 2048
+    big = torch.exp2(3.0 + 10.0 * torch.rand(2048, generator=g, device="cuda"))  # [8, 8192)
+    logits[0, torch.tensor(pos, device="cuda")] = big
+    L = torch.tensor([Lr], dtype=torch.int32, device="cuda")
+    sel = gpu_topk(logits, Lr, L, 2048)
+    sets_equal(sel, logits, L, 2048)
+    assert sorted(np_(sel)[0].tolist()) == sorted(pos)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_device_error(clear=True) == dsa.DEVERR_CAPACITY
+
+
 def test_topk_small_k_and_odd_sizes():
     g = torch.Generator(device="cuda").manual_seed(3)
     L = torch.tensor([3, 10, 17, 1000], dtype=torch.int32, device="cuda")
