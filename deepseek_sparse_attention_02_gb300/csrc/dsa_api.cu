@@ -365,9 +365,19 @@ dsa_status dsa_topk_hist(const float* logits, int64_t ld, const int32_t* row_len
                         hist, stream);
 }
 
+// The SM count the sparse MLA's work split is sized for: the current
+// device's, or GB300's 152 when no device can be queried (a size asked for on
+// a machine without a GPU).
+static int mla_sm_count() {
+  DeviceInfo dev;
+  if (current_device_info(&dev) == cudaSuccess && dev.sm_count > 0) return dev.sm_count;
+  cudaGetLastError();  // the failed query leaves no sticky error for later calls
+  return 152;
+}
+
 size_t dsa_sparse_mla_workspace_size(int R, int k) {
   if (R <= 0 || k <= 0) return 0;
-  return mla_workspace_size(R, k);
+  return mla_workspace_size(R, k, mla_sm_count());
 }
 
 dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache,
@@ -394,13 +404,13 @@ dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache,
   if (R64 > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
   const int R = static_cast<int>(R64);
   if (R == 0) return ok();
-  const size_t need = mla_workspace_size(R, k);
-  if (need > 0 && (!workspace || workspace_bytes < need))
-    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
-                workspace_bytes);
   DeviceInfo dev;
   dsa_status st = device_ready(&dev);
   if (st != DSA_OK) return st;
+  const size_t need = mla_workspace_size(R, k, dev.sm_count);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace_bytes);
   MlaArgs a{q,   kv_cache, kv_page_stride, num_pages, block_table, bt_stride, num_req, next_n,
             idx, k,        sm_scale,       out,       lse,         workspace, workspace_bytes};
   return cuda_status(launch_sparse_mla(a, dev, static_cast<cudaStream_t>(stream)), fn);
@@ -491,13 +501,13 @@ dsa_status dsa_sparse_mla_decode_varlen(const uint16_t* q, const uint16_t* kv_ca
     return fail(DSA_ERR_UNSUPPORTED, "%s: more than 2^31 cached latent rows", fn);
   if (R > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
   if (R == 0) return ok();
-  const size_t need = mla_workspace_size(R, k);
-  if (need > 0 && (!workspace || workspace_bytes < need))
-    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
-                workspace_bytes);
   DeviceInfo dev;
   dsa_status st = device_ready(&dev);
   if (st != DSA_OK) return st;
+  const size_t need = mla_workspace_size(R, k, dev.sm_count);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(DSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace_bytes);
   MlaArgs a{q,   kv_cache, kv_page_stride, num_pages, block_table, bt_stride, 1,         1,
             idx, k,        sm_scale,       out,       lse,         workspace, workspace_bytes};
   a.row_bt = row_bt;
@@ -534,7 +544,7 @@ dsa_status dsa_sparse_mla_decode_static(const uint16_t* q, const uint16_t* kv_ca
   DeviceInfo dev;
   dsa_status st = device_ready(&dev);
   if (st != DSA_OK) return st;
-  const size_t need = mla_workspace_size(static_cast<int>(R64), k);
+  const size_t need = mla_workspace_size(static_cast<int>(R64), k, dev.sm_count);
   if (need > mla_static_scratch_bytes())
     return fail(DSA_ERR_UNSUPPORTED,
                 "%s: this batch needs %zu bytes of split-K scratch but the static scratch holds "

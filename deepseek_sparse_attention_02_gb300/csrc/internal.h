@@ -104,7 +104,9 @@ struct MlaArgs {
   int rows = 0;
 };
 
-size_t mla_workspace_size(int R, int k);
+// Split-K partials of R rows x k selections on a device with sm_count SMs
+// (the split count follows the SM count).
+size_t mla_workspace_size(int R, int k, int sm_count);
 cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // No-allocation variant: split-K scratch from a static device array.  The

@@ -73,7 +73,6 @@ constexpr int kChunksV = 8;  // 512 / 64: value chunks per tile (value CTA)
 constexpr int kHeads = 128;
 constexpr int kDqk = 576;
 constexpr int kHalf = 256;   // columns of one partial-O block of the combine kernel
-constexpr int kTargetCtas = 152;
 constexpr uint32_t kChunkBytes = kTile * 128;  // 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -789,24 +788,26 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MParams p) {
         __bfloat16_as_ushort(__float2bfloat16_rn(acc[j] * inv_l[j]));
 }
 
-int choose_nsplit(int R, int k) {
+// Splits of each row's selections: doubled while the CTA pairs of all rows
+// and splits (2 R ns CTAs) still fit the device's SMs in one wave.
+int choose_nsplit(int R, int k, int sm_count) {
   int ns = 1;
   const int max_split = (k + kTile - 1) / kTile;
-  while (2 * R * ns * 2 <= kTargetCtas && ns * 2 <= max_split && ns * 2 <= 64) ns *= 2;
+  while (2 * R * ns * 2 <= sm_count && ns * 2 <= max_split && ns * 2 <= 64) ns *= 2;
   return ns;
 }
 
 }  // namespace
 
-size_t mla_workspace_size(int R, int k) {
-  const int ns = choose_nsplit(R, k);
+size_t mla_workspace_size(int R, int k, int sm_count) {
+  const int ns = choose_nsplit(R, k, sm_count);
   if (ns == 1) return 0;
   return static_cast<size_t>(R) * 2 * ns * (kHeads * kHalf + 2 * kHeads) * sizeof(float);
 }
 
 cudaError_t launch_sparse_mla(const MlaArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   const int R = a.row_bt ? a.rows : a.num_req * a.next_n;
-  const int ns = choose_nsplit(R, a.k);
+  const int ns = choose_nsplit(R, a.k, dev.sm_count);
   const int tiles = (a.k + kTile - 1) / kTile;
   const int tps = ((tiles + ns - 1) / ns) * kTile;
   MParams p;
@@ -910,7 +911,7 @@ cudaError_t launch_sparse_mla_static(const MlaArgs& a_in, const DeviceInfo& dev,
   const cudaError_t e = static_scratch_address(dev.device, &ptr);
   if (e != cudaSuccess) return e;
   const int R = a_in.row_bt ? a_in.rows : a_in.num_req * a_in.next_n;
-  const size_t need = mla_workspace_size(R, a_in.k);
+  const size_t need = mla_workspace_size(R, a_in.k, dev.sm_count);
   if (need > kStaticScratchBytes) return cudaErrorInvalidValue;  // the caller checks first
   MlaArgs a = a_in;
   a.ws = need > 0 ? ptr : nullptr;

@@ -227,6 +227,12 @@ dsa_status dsa_topk_bf16(const uint16_t* logits, int64_t ld, const int32_t* row_
  *   out       device [R, 128, 512] bf16.   lse  device [R, 128] f32 (may be NULL).
  *   workspace device, dsa_sparse_mla_workspace_size(R, k) bytes (split-K
  *             partial results; may be NULL when that size is 0).
+ *
+ * The rows' selections are split (split-K) only while the CTA pairs of all
+ * rows and splits still fit the device's SMs in one wave, so the workspace
+ * size depends on the SM count of the device current when it is asked for
+ * (152 on GB300; 152 is also assumed when no device can be queried): ask on
+ * the device that will run the call.
  * ---------------------------------------------------------------------- */
 size_t dsa_sparse_mla_workspace_size(int R, int k);
 
